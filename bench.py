@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of the tree-verify MLA attention path (one JSON line on rank 0).
+
+A step is one call of mla_verify_attn (prep -> fused verify -> split combine)
+over one batch of synthetic inputs resident in HBM.  Default workload: 16
+requests x prefix 16384 x 32-node draft trees, 64 heads, paged KV (page 64,
+random block table) -- the uniform workload at the prefix length where the
+roofline target applies.  ``--workload`` selects another one.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3] [--splits S]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+For N > 1 (torchrun) every rank runs an independent replica of the workload
+on its own GPU (the path has no exchange step); value = all ranks' work over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn TFLOP/s & KV GB/s, % of roofline, 1 GB300, prefix 4k-64k"
+WORKLOADS = {"c2": 2, "c3": 3, "c4": 4, "c5": 5}
+DEFAULT_SPLITS = {"c4": 16}
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
+    ap.add_argument("--splits", type=int, default=None, help="KV splits (0 = library's choice)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows timed for cpu_baseline")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    a.steps = max(a.steps, 1)
+    if a.splits is None:
+        a.splits = DEFAULT_SPLITS.get(a.workload, 0)
+    return a
+
+
+# ------------------------------------------------------------------ ranks
+
+class Ranks:
+    """Rank bookkeeping for torchrun launches (replicas; barrier + max only)."""
+
+    def __init__(self, backend="nccl"):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                import torch
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, value: float, device=None) -> float:
+        if self.dist is None:
+            return float(value)
+        import torch
+        t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        power = [num(r[3]) or 0.0 for r in rows]
+        pmax = max(power)
+        loaded = [r for r, p in zip(rows, power) if p >= 0.5 * pmax] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(loaded), "power_w_max": pmax}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(workload: str, launch_units: int):
+    """DRAM bytes per launch of the fused verify kernel from the committed ncu
+    summary, if it was taken on the current kernel sources (else None)."""
+    from mla_speculative_decoding_verify_gb300 import metrics
+    path = os.path.join(ROOT, "profiles", "verify_kernel_dram.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != metrics.kernel_source_hash():
+        return None
+    entry = d.get("workloads", {}).get(workload)
+    if not entry:
+        return None
+    # scale a smaller capture to one full launch by the units processed
+    return int(entry["dram_bytes_per_launch"] * launch_units / entry.get("units", launch_units))
+
+
+def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7):
+    import numpy as np
+
+    import oracle
+    from mla_speculative_decoding_verify_gb300 import inputs as I
+    sample = I.sample_rows(inp, rows, seed=seed)
+    t0 = time.perf_counter()
+    oracle.verify_rows(inp, sample)
+    dt = time.perf_counter() - t0
+    total_rows = inp.total_q * inp.num_heads
+    # flops of the sampled rows: rows share their request's key count
+    per_row = flops_total / total_rows
+    value = per_row * len(sample) / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(sample)} of {total_rows} output rows, fp64 C oracle, all host threads, "
+                      f"{dt:.2f} s wall"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, ranks: Ranks):
+    import numpy as np
+    import torch
+
+    from mla_speculative_decoding_verify_gb300 import binding, inputs as I, metrics
+
+    dev = torch.device(f"cuda:{ranks.local}")
+    torch.cuda.set_device(dev)
+    binding.init(ranks.local)
+    cfg = WORKLOADS[args.workload]
+    inp = I.config_inputs(cfg, seed=args.seed)
+    flops = metrics.algorithmic_flops(inp)
+    kv_logical = metrics.kv_bytes(inp)
+    kv_unique = metrics.kv_bytes(inp, unique=True)
+    io = metrics.io_bytes(inp)
+    db = binding.DeviceBatch(inp, dev)
+    splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
+                                args.splits)
+    out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
+                                            inp.num_heads, splits), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    status = binding.read_status(ws.data_ptr())
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(ranks.local)
+    clocks.start()
+    time.sleep(0.3)
+    ranks.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()                      # L2 flush between timed steps (not timed)
+        binding.set_profile_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    binding.set_profile_events(None, None)
+    torch.cuda.synchronize(dev)
+    ranks.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    t_step = ranks.max(sum(step_ms) / K, dev)
+    t_kern = ranks.max(sum(kern_ms) / K, dev)
+    launches = (3 if splits > 1 else 2) * K
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        def pin(a, dt):
+            return torch.from_numpy(np.ascontiguousarray(a).view(dt)).pin_memory()
+        h = dict(q_lat=pin(inp.q_lat, np.int16), q_rope=pin(inp.q_rope, np.int16),
+                 kv_cache=pin(inp.kv_cache, np.int16), block_table=pin(inp.block_table, np.int32),
+                 seq_lens=pin(inp.seq_lens, np.int32), tree_parent=pin(inp.tree_parent, np.int32),
+                 n_tree=pin(inp.n_tree, np.int32))
+        h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for k, t in h.items():
+                getattr(db, k).copy_(t, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+        for _ in range(args.warmup):
+            flush.zero_()
+            e2e_step()
+        K2 = max(5, K // 4)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+        ranks.barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(K2):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            e2e_step()
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ranks.barrier()
+        t_e2e = ranks.max(sum(a.elapsed_time(b) for a, b in ev2) / K2, dev)
+        e2e = {"value": ranks.world * flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"], "ms_per_step": t_e2e,
+               "steps": K2}
+        launches += 0  # e2e steps are outside the kernel-timed region
+
+    status = binding.read_status(ws.data_ptr())
+    peaks, peak_kind = measured_peaks()
+    achieved = flops / (t_kern * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    # units of one launch = (row tile, split) work units
+    units = ((inp.n_tree + 1) // 2).sum() * splits
+    traffic = profiled_traffic(args.workload, int(units))
+    result = {
+        "metric": METRIC,
+        "value": ranks.world * flops / (t_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": ranks.world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": t_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": inp.name, "batch": inp.batch, "prefix": int(inp.prefix_lens.max()),
+                   "tree": int(inp.max_tree), "heads": inp.num_heads, "d_latent": 512, "d_rope": 64,
+                   "page_size": inp.page_size, "num_splits": splits, "seed": args.seed,
+                   "parallelism": f"replicas x{ranks.world}",
+                   "l2": "flushed between timed steps (256 MiB write, not timed)"},
+        "kv_gbps": {"logical": kv_logical / (t_step * 1e-3) / 1e9, "unique": kv_unique / (t_step * 1e-3) / 1e9,
+                    "hbm_peak": float(peaks["hbm_gbs"])},
+        "algorithmic_gflop_per_step": flops / 1e9,
+        "kernel_ms": t_kern,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16_tflops (burst), MEASURED_PEAKS.json"
+                     if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "mla_verify_kernel", "flops_per_launch": flops},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if ranks.rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, flops, args.cpu_rows)
+    return result
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, ranks: Ranks):
+    """The fp64 oracle, as it stands, on the host cores: each step evaluates a
+    bounded seeded sample of the workload's output rows."""
+    import oracle
+    from mla_speculative_decoding_verify_gb300 import inputs as I, metrics
+    cfg = WORKLOADS[args.workload]
+    inp = I.config_inputs(cfg, seed=args.seed)
+    flops = metrics.algorithmic_flops(inp)
+    total_rows = inp.total_q * inp.num_heads
+    per_row = flops / total_rows
+    rows_per_step = 128
+    oracle.build()
+    times = []
+    for i in range(args.warmup + args.steps):
+        sample = I.sample_rows(inp, rows_per_step, seed=1000 + i)
+        t0 = time.perf_counter()
+        oracle.verify_rows(inp, sample)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append((dt, len(sample)))
+    t = sum(d for d, _ in times)
+    n = sum(k for _, k in times)
+    value = per_row * n / t / 1e12
+    ms_per_step = t / len(times) * 1e3
+    sample_desc = f"{rows_per_step}+ of {total_rows} output rows per step, fp64 C oracle, all host threads"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": inp.name, "batch": inp.batch, "prefix": int(inp.prefix_lens.max()),
+                   "tree": int(inp.max_tree), "heads": inp.num_heads, "page_size": inp.page_size},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, _single())), flush=True)
+        return 0
+    ranks = Ranks("nccl")
+    try:
+        res = run_ours(args, ranks)
+        if ranks.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        ranks.close()
+    return 0
+
+
+def _single():
+    r = Ranks.__new__(Ranks)
+    r.rank, r.world, r.local, r.dist = 0, int(os.environ.get("WORLD_SIZE", "1")), 0, None
+    return r
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,173 @@
+/*
+ * mla_verify.h -- C ABI of the GB300 (sm_103a) MLA tree-verify attention library.
+ *
+ * The operation ("verify attention" of tree speculative decoding, page "The
+ * Shared Memory Ceiling", sections "The Broader Context" and "Technical Deep
+ * Dive"): every draft-tree token of a request, in each of 64 heads, attends
+ * to the request's latent KV cache.  A KV row is a 512-dim c_kv latent
+ * followed by a 64-dim k_rope; all heads share it; V is the c_kv latent.  A
+ * tree token sees the whole prefix and, among the tree's own latents, only
+ * its ancestors and itself (given by a parent array).  The softmax is taken
+ * online, tile by tile, so no full score row is ever held (same page,
+ * "Technical Deep Dive", last paragraph).  Long prefixes with few requests
+ * may be split along the KV axis and merged with log-sum-exp weights.
+ *
+ * Conventions of every call:
+ *  - Pointers marked "device" are device memory owned by the caller; the
+ *    library never frees, reallocates or retains them past the call.  bf16
+ *    tensors are passed as raw 16-bit patterns (const void*).
+ *  - Work is enqueued on the caller's stream; no call synchronises the host
+ *    except mla_read_status().  mla_verify_attn and mla_split_combine
+ *    allocate nothing; they are safe to capture in a CUDA graph once
+ *    mla_init() has run on the device.
+ *  - Every call returns an mla_status.  Errors detectable from the scalar
+ *    arguments are returned before anything is launched.  Errors that depend
+ *    on device data (an invalid tree, a block id outside the cache, a
+ *    pipeline wait that timed out) are recorded in a status word inside the
+ *    workspace; read it with mla_read_status().  Rows of a request with
+ *    invalid data are written as out = 0, lse = -inf; no kernel traps.
+ *  - Supported shapes: num_heads = 64, d_latent = 512, d_rope = 64,
+ *    page_size a positive multiple of 64, 1 <= n_tree[b] <= 64 (or 0 for an
+ *    empty request), bf16 inputs, fp32 outputs.  Anything else returns
+ *    MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_VERIFY_H_
+#define MLA_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer  */
+    MLA_ERR_UNSUPPORTED = 2,  /* shape outside the supported set above            */
+    MLA_ERR_WORKSPACE = 3,    /* workspace null or smaller than required           */
+    MLA_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed               */
+    MLA_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (status word)  */
+    MLA_ERR_BAD_TREE = 6,     /* parent outside [-1, i), n_tree > seq_len, sums    */
+    MLA_ERR_BAD_BLOCK = 7,    /* block-table entry outside [0, num_pages)          */
+    MLA_ERR_NOT_INITIALIZED = 8 /* mla_init() has not run on the current device    */
+} mla_status;
+
+#define MLA_NUM_HEADS 64
+#define MLA_D_LATENT 512
+#define MLA_D_ROPE 64
+#define MLA_MAX_TREE 64
+#define MLA_MAX_SPLITS 64
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int mla_version(void);
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char *mla_error_string(int status);
+
+/*
+ * Per-device set-up: checks that `device` is an sm_103 GPU, raises the
+ * kernels' dynamic shared-memory limit and resolves the driver's tensor-map
+ * encoder.  Call once per device, outside stream capture, before the first
+ * verify call on that device.  Makes `device` current.  Idempotent.
+ */
+int mla_init(int device);
+
+/*
+ * Number of KV splits the verify call will use.  `requested` > 0 is honoured
+ * (clamped to [1, MLA_MAX_SPLITS]); 0 picks one from the shape: enough
+ * (request, row-tile, split) work units to fill every SM of the current
+ * device in whole waves, with at least 16 KV tiles of 64 keys per split.
+ * Returns the count, or a negative mla_status on invalid arguments.
+ */
+int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
+                          int num_heads, int requested);
+
+/*
+ * Bytes of device workspace mla_verify_attn needs for these sizes (with
+ * `num_splits` resolved as by mla_verify_num_splits).  0 on invalid input.
+ */
+size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_seq_len,
+                                 int num_heads, int num_splits);
+
+/*
+ * Tree-verify attention over a paged latent KV cache.
+ *
+ *  q_lat       device bf16 [total_q, num_heads, 512]   query in the latent space
+ *  q_rope      device bf16 [total_q, num_heads, 64]    rotary part of the query
+ *  kv_cache    device bf16 [num_pages, page_size, 576] row = c_kv (512) | k_rope (64)
+ *  block_table device int32 [batch, max_pages_per_seq]  page of KV position t of
+ *              request b is block_table[b][t / page_size], row t % page_size
+ *  seq_lens    device int32 [batch]  KV rows of request b = prefix_b + n_tree[b];
+ *              the tree tokens' own latents occupy positions prefix_b .. seq_len-1
+ *  tree_parent device int32 [total_q] request-local parent of each tree token,
+ *              -1 for a root (child of the last prefix token); parent[i] < i
+ *  n_tree      device int32 [batch]  tree tokens of each request; requests are
+ *              laid out back to back in q_lat / tree_parent / out
+ *  scale       softmax scale applied to q . k (latent and rope parts alike)
+ *  out         device fp32 [total_q, num_heads, 512]  softmax-weighted c_kv
+ *  lse         device fp32 [total_q, num_heads]  natural-log log-sum-exp of the
+ *              scaled scores over the visible keys
+ *  stream      stream the work is enqueued on
+ *  batch, total_q      sizes of the arrays above (total_q = sum of n_tree)
+ *  max_tree, max_seq_len  host-side upper bounds of n_tree[b] and seq_lens[b]
+ *  num_heads   must be 64
+ *  page_size   rows per page, a multiple of 64
+ *  num_pages   pages in kv_cache (block ids must lie in [0, num_pages))
+ *  max_pages_per_seq  row stride of block_table
+ *  num_splits  KV splits (0 = choose, see mla_verify_num_splits)
+ *  workspace   device scratch of at least mla_verify_workspace_size(...) bytes,
+ *              256-byte aligned; it holds the status word, the per-call tree
+ *              metadata and, when split, the partial outputs.  Its contents
+ *              are owned by the library until the stream reaches the end of
+ *              the call; do not share one workspace between calls that may run
+ *              concurrently.
+ *
+ * Pointer alignment: bf16/fp32 tensors 16-byte aligned.  The result does not
+ * depend on how pages are placed in the pool (only on the logical rows), and
+ * repeated calls with the same inputs give bitwise-identical results.
+ */
+int mla_verify_attn(const void *q_lat, const void *q_rope, const void *kv_cache,
+                    const int32_t *block_table, const int32_t *seq_lens,
+                    const int32_t *tree_parent, const int32_t *n_tree, float scale,
+                    float *out, float *lse, cudaStream_t stream,
+                    int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
+                    int page_size, int num_pages, int max_pages_per_seq, int num_splits,
+                    void *workspace, size_t workspace_bytes);
+
+/*
+ * Log-sum-exp merge of split-KV partials (flash-decoding combine).
+ *
+ *  part_out  device fp32 [num_splits, rows, 512]  each split's normalised output
+ *  part_lse  device fp32 [num_splits, rows]       each split's natural-log LSE;
+ *            -inf marks a split that saw no key (weight 0)
+ *  out       device fp32 [rows, 512]:  sum_s exp(lse_s - lse) * part_out[s]
+ *  lse       device fp32 [rows]:       max_s lse_s + ln sum_s exp(lse_s - max_s lse_s)
+ * A row whose partials are all -inf gets out = 0, lse = -inf.
+ * 1 <= num_splits <= MLA_MAX_SPLITS; pointers 16-byte aligned.
+ */
+int mla_split_combine(const float *part_out, const float *part_lse, int num_splits, int rows,
+                      float *out, float *lse, cudaStream_t stream);
+
+/*
+ * Measurement hook: while set, every mla_verify_attn call records `begin`
+ * immediately before and `end` immediately after the launch of its fused
+ * verify kernel, on the call's stream, so the kernel can be timed alone.
+ * Pass NULL, NULL to stop.  Process-wide setting; not thread-safe.
+ */
+int mla_set_profile_events(cudaEvent_t begin, cudaEvent_t end);
+
+/*
+ * Synchronously read the device status word of the last call that used
+ * `workspace` (waits for the device).  *device_status receives a bit mask:
+ * bit k set means status code k was raised (e.g. 1 << MLA_ERR_BAD_TREE).
+ * Returns MLA_OK if the word was read, MLA_ERR_CUDA otherwise.
+ */
+int mla_read_status(const void *workspace, int *device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_VERIFY_H_ */

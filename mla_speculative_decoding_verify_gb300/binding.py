@@ -1,0 +1,183 @@
+"""ctypes binding of libmla_verify.so (the C ABI in include/mla_verify.h).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+library.  torch is used for device memory and streams.  If the compiled
+library is missing, every entry point raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libmla_verify.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = 1
+MLA_ERR_UNSUPPORTED = 2
+MLA_ERR_WORKSPACE = 3
+MLA_ERR_CUDA = 4
+MLA_ERR_TIMEOUT = 5
+MLA_ERR_BAD_TREE = 6
+MLA_ERR_BAD_BLOCK = 7
+MLA_ERR_NOT_INITIALIZED = 8
+
+NUM_HEADS = 64
+D_LATENT = 512
+D_ROPE = 64
+MAX_TREE = 64
+MAX_SPLITS = 64
+
+EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
+            "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
+            "mla_read_status", "mla_set_profile_events")
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        msg = error_string(code) if _lib is not None else str(code)
+        super().__init__(f"{what}: status {code} ({msg})" if what else f"status {code} ({msg})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load the compiled library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_NAME} is not built (expected at {LIB_PATH}); "
+                               "run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.mla_version.restype = i32
+        L.mla_error_string.restype = ctypes.c_char_p
+        L.mla_error_string.argtypes = [i32]
+        L.mla_init.restype = i32
+        L.mla_init.argtypes = [i32]
+        L.mla_verify_num_splits.restype = i32
+        L.mla_verify_num_splits.argtypes = [i32] * 6
+        L.mla_verify_workspace_size.restype = sz
+        L.mla_verify_workspace_size.argtypes = [i32] * 6
+        L.mla_verify_attn.restype = i32
+        L.mla_verify_attn.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                      i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz]
+        L.mla_split_combine.restype = i32
+        L.mla_split_combine.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+        L.mla_set_profile_events.restype = i32
+        L.mla_set_profile_events.argtypes = [vp, vp]
+        L.mla_read_status.restype = i32
+        L.mla_read_status.argtypes = [vp, ctypes.POINTER(i32)]
+        _lib = L
+        return L
+
+
+def error_string(code: int) -> str:
+    return lib().mla_error_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(lib().mla_version())
+
+
+def check(code: int, what: str = "") -> None:
+    if code != MLA_OK:
+        raise MlaError(code, what)
+
+
+def init(device: int = 0) -> None:
+    check(lib().mla_init(int(device)), "mla_init")
+
+
+def num_splits(batch, total_q, max_tree, max_seq_len, num_heads=NUM_HEADS, requested=0) -> int:
+    s = lib().mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, requested)
+    if s <= 0:
+        raise MlaError(-s, "mla_verify_num_splits")
+    return int(s)
+
+
+def workspace_size(batch, total_q, max_tree, max_seq_len, num_heads=NUM_HEADS, splits=0) -> int:
+    return int(lib().mla_verify_workspace_size(batch, total_q, max_tree, max_seq_len, num_heads,
+                                               splits))
+
+
+def verify_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale,
+                out, lse, stream, batch, total_q, max_tree, max_seq_len, num_heads, page_size,
+                num_pages, max_pages_per_seq, num_splits, workspace, workspace_bytes) -> int:
+    """Raw call with integer pointers; returns the mla_status code."""
+    return int(lib().mla_verify_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent,
+                                     n_tree, float(scale), out, lse, stream, batch, total_q,
+                                     max_tree, max_seq_len, num_heads, page_size, num_pages,
+                                     max_pages_per_seq, num_splits, workspace, workspace_bytes))
+
+
+def split_combine(part_out, part_lse, num_splits, rows, out, lse, stream) -> int:
+    return int(lib().mla_split_combine(part_out, part_lse, num_splits, rows, out, lse, stream))
+
+
+def set_profile_events(begin, end) -> None:
+    """Record CUDA events (raw cudaEvent_t handles) around the fused verify kernel."""
+    check(lib().mla_set_profile_events(begin, end), "mla_set_profile_events")
+
+
+def read_status(workspace) -> int:
+    v = ctypes.c_int(0)
+    check(lib().mla_read_status(workspace, ctypes.byref(v)), "mla_read_status")
+    return int(v.value)
+
+
+# ---------------------------------------------------------------- torch glue
+
+class DeviceBatch:
+    """A batch of verify inputs resident on the GPU (torch tensors, bf16 as int16 bits)."""
+
+    def __init__(self, inp, device="cuda", pin: bool = False):
+        import numpy as np
+        import torch
+        self.inp = inp
+        dev = torch.device(device)
+
+        def up(a, dtype):
+            t = torch.from_numpy(np.ascontiguousarray(a).view(dtype))
+            return t.to(dev, non_blocking=False)
+        self.q_lat = up(inp.q_lat, np.int16)
+        self.q_rope = up(inp.q_rope, np.int16)
+        self.kv_cache = up(inp.kv_cache, np.int16)
+        self.block_table = up(inp.block_table, np.int32)
+        self.seq_lens = up(inp.seq_lens, np.int32)
+        self.tree_parent = up(inp.tree_parent, np.int32)
+        self.n_tree = up(inp.n_tree, np.int32)
+        self.device = dev
+
+
+def verify(db: "DeviceBatch", num_splits_req: int = 0, out=None, lse=None, workspace=None,
+           stream=None, max_tree: Optional[int] = None, max_seq_len: Optional[int] = None):
+    """Run mla_verify_attn on a DeviceBatch; returns (out [total_q, 64, 512], lse [total_q, 64])."""
+    import torch
+    inp = db.inp
+    mt = inp.max_tree if max_tree is None else max_tree
+    ms = inp.max_seq_len if max_seq_len is None else max_seq_len
+    if out is None:
+        out = torch.empty((inp.total_q, inp.num_heads, D_LATENT), dtype=torch.float32, device=db.device)
+    if lse is None:
+        lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=db.device)
+    need = workspace_size(inp.batch, inp.total_q, mt, ms, inp.num_heads, num_splits_req)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=db.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(db.device)
+    code = verify_attn(db.q_lat.data_ptr(), db.q_rope.data_ptr(), db.kv_cache.data_ptr(),
+                       db.block_table.data_ptr(), db.seq_lens.data_ptr(), db.tree_parent.data_ptr(),
+                       db.n_tree.data_ptr(), inp.scale, out.data_ptr(), lse.data_ptr(),
+                       stream.cuda_stream, inp.batch, inp.total_q, mt, ms, inp.num_heads,
+                       inp.page_size, inp.num_pages, inp.max_pages_per_seq, num_splits_req,
+                       workspace.data_ptr(), workspace.numel())
+    check(code, "mla_verify_attn")
+    return out, lse, workspace

@@ -1,0 +1,332 @@
+// Host side of the C ABI declared in include/mla_verify.h: argument checks,
+// per-device set-up, TMA descriptor encoding, the split heuristic, workspace
+// layout and the launches (prep -> verify -> combine) on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "mla_verify.h"
+#include "combine_kernel.cuh"
+#include "prep_kernel.cuh"
+#include "verify_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per pipeline wait
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+// Workspace layout shared by the size query and the launch.
+struct Layout {
+    size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, total;
+    int max_items;
+};
+
+Layout make_layout(int batch, int total_q, int num_splits) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.max_items = (total_q + batch) / 2 + 1;
+    L.status = take(sizeof(int));
+    L.item_count = take(sizeof(int));
+    L.q_off = take(sizeof(int32_t) * (batch + 1));
+    L.req_state = take(sizeof(int32_t) * batch);
+    L.order = take(sizeof(int32_t) * batch);
+    L.item_off = take(sizeof(int32_t) * (batch + 1));
+    L.anc = take(sizeof(uint64_t) * (total_q > 0 ? total_q : 1));
+    L.items = take(sizeof(int2) * L.max_items);
+    const size_t rows = static_cast<size_t>(total_q) * MLA_NUM_HEADS;
+    if (num_splits > 1) {
+        L.part_out = take(sizeof(float) * rows * MLA_D_LATENT * num_splits);
+        L.part_lse = take(sizeof(float) * rows * num_splits);
+    } else {
+        L.part_out = L.part_lse = 0;
+    }
+    L.total = off;
+    return L;
+}
+
+int sm_count_of_current() {
+    const int d = current_device();
+    if (d >= 0 && d < kMaxDevices && g_dev[d].ready) return g_dev[d].sm_count;
+    int n = 0;
+    if (d >= 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) == cudaSuccess && n > 0) return n;
+    return 152;
+}
+
+// Model of the verify time (in KV-tile units of one CTA pair) for `splits`
+// splits: whole waves of (request, row tile, split) units over the SMs,
+// a fixed per-unit cost, and the combine pass when split.
+double model_time(long long units_per_split, int tiles, int splits, int pairs, long long rows) {
+    const double kUnitOverheadTiles = 6.0;  // q load, pipeline fill, epilogue
+    const double kTileSeconds = 1.1e-6;     // one 64-key tile of 128 rows on a CTA pair
+    const double kCombineBytesPerSecond = 5.0e12;
+    const long long units = units_per_split * splits;
+    const long long waves = (units + pairs - 1) / pairs;
+    const double per_unit = std::ceil(static_cast<double>(tiles) / splits) + kUnitOverheadTiles;
+    double t = static_cast<double>(waves) * per_unit;
+    if (splits > 1) t += (static_cast<double>(rows) * splits * 2048.0 / kCombineBytesPerSecond) / kTileSeconds;
+    return t;
+}
+
+int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
+    const long long items_bound = std::min<long long>(static_cast<long long>(batch) * ((max_tree + 1) / 2),
+                                                      (static_cast<long long>(total_q) + batch) / 2);
+    const int tiles = (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
+    const int pairs = sm_count_of_current() / 2;
+    const long long rows = static_cast<long long>(total_q) * MLA_NUM_HEADS;
+    const int max_s = std::max(1, std::min(MLA_MAX_SPLITS, tiles / 16));
+    int best = 1;
+    double best_t = model_time(items_bound, tiles, 1, pairs, rows);
+    for (int s = 2; s <= max_s; ++s) {
+        const double t = model_time(items_bound, tiles, s, pairs, rows);
+        if (t < best_t * 0.97) {  // prefer fewer splits unless clearly faster
+            best_t = t;
+            best = s;
+        }
+    }
+    return best;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int encode_maps(const void* kv_cache, long long rows, CUtensorMap* lat, CUtensorMap* rope) {
+    if (!g_encode) return MLA_ERR_NOT_INITIALIZED;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLA_D_LATENT + MLA_D_ROPE), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>((MLA_D_LATENT + MLA_D_ROPE) * 2)};
+    const cuuint32_t box_lat[2] = {64, static_cast<cuuint32_t>(mla::kBlockN)};
+    const cuuint32_t box_rope[2] = {static_cast<cuuint32_t>(mla::kDRopeHalf), static_cast<cuuint32_t>(mla::kBlockN)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r1 = g_encode(lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims, strides,
+                           box_lat, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r2 = g_encode(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims, strides,
+                           box_rope, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS) ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int launch_combine(const float* part_out, const float* part_lse, int num_splits, long long rows, float* out,
+                   float* lse, cudaStream_t stream) {
+    if (rows == 0) return MLA_OK;
+    const long long blocks = (rows + mla::kCombineWarps - 1) / mla::kCombineWarps;
+    mla::mla_combine_kernel<<<static_cast<unsigned>(blocks), mla::kCombineWarps * 32, 0, stream>>>(
+        part_out, part_lse, num_splits, rows, out, lse);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char* mla_error_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape";
+        case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_TIMEOUT: return "device-side wait timed out";
+        case MLA_ERR_BAD_TREE: return "invalid draft tree or lengths";
+        case MLA_ERR_BAD_BLOCK: return "block-table entry out of range";
+        case MLA_ERR_NOT_INITIALIZED: return "mla_init has not run on this device";
+        default: return "unknown status";
+    }
+}
+
+int mla_init(int device) {
+    if (device < 0 || device >= kMaxDevices) return MLA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
+    if (g_dev[device].ready) return MLA_OK;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MLA_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MLA_ERR_UNSUPPORTED;  // built for sm_103a only
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return MLA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaFuncSetAttribute(mla::mla_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    g_dev[device].sm_count = prop.multiProcessorCount;
+    g_dev[device].ready = true;
+    return MLA_OK;
+}
+
+int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len, int num_heads, int requested) {
+    if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || requested < 0) return -MLA_ERR_INVALID_ARG;
+    if (num_heads != MLA_NUM_HEADS) return -MLA_ERR_UNSUPPORTED;
+    if (requested > 0) return std::min(requested, MLA_MAX_SPLITS);
+    return choose_splits(batch, total_q, max_tree, max_seq_len);
+}
+
+size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
+                                 int num_splits) {
+    const int s = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
+    if (s <= 0) return 0;
+    return make_layout(batch, total_q, s).total;
+}
+
+int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, const int32_t* tree_parent, const int32_t* n_tree, float scale,
+                    float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
+                    int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                    int num_splits, void* workspace, size_t workspace_bytes) {
+    // ---- host-checkable arguments ----
+    if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
+        num_splits < 0 || page_size <= 0 || !std::isfinite(scale))
+        return MLA_ERR_INVALID_ARG;
+    if (num_heads != MLA_NUM_HEADS || page_size % mla::kBlockN != 0 || max_tree > MLA_MAX_TREE ||
+        num_splits > MLA_MAX_SPLITS)
+        return MLA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0) return MLA_OK;  // nothing to compute
+    if (!q_lat || !q_rope || !kv_cache || !block_table || !seq_lens || !tree_parent || !n_tree || !out || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    if (num_pages == 0 || max_pages_per_seq == 0) return MLA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MLA_ERR_NOT_INITIALIZED;
+    const int splits = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
+    if (splits <= 0) return MLA_ERR_INVALID_ARG;
+    const Layout lay = make_layout(batch, total_q, splits);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MLA_ERR_WORKSPACE;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws + lay.status);
+    int32_t* item_count = reinterpret_cast<int32_t*>(ws + lay.item_count);
+    int32_t* q_off = reinterpret_cast<int32_t*>(ws + lay.q_off);
+    int32_t* req_state = reinterpret_cast<int32_t*>(ws + lay.req_state);
+    uint64_t* anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
+    int2* items = reinterpret_cast<int2*>(ws + lay.items);
+    float* part_out = splits > 1 ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
+    float* part_lse = splits > 1 ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+
+    CUtensorMap map_lat, map_rope;
+    const int enc = encode_maps(kv_cache, static_cast<long long>(num_pages) * page_size, &map_lat, &map_rope);
+    if (enc != MLA_OK) return enc;
+
+    // ---- prep: offsets, ancestor bit sets, validation, work list ----
+    mla::PrepParams pp{};
+    pp.block_table = block_table;
+    pp.seq_lens = seq_lens;
+    pp.tree_parent = tree_parent;
+    pp.n_tree = n_tree;
+    pp.q_off = q_off;
+    pp.req_state = req_state;
+    pp.order = reinterpret_cast<int32_t*>(ws + lay.order);
+    pp.item_off = reinterpret_cast<int32_t*>(ws + lay.item_off);
+    pp.anc = anc;
+    pp.items = items;
+    pp.item_count = item_count;
+    pp.status = status;
+    pp.batch = batch;
+    pp.total_q = total_q;
+    pp.page_size = page_size;
+    pp.max_pages = max_pages_per_seq;
+    pp.num_pages = num_pages;
+    pp.max_items = lay.max_items;
+    mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+    // ---- fused verify attention ----
+    mla::VerifyParams vp{};
+    vp.q_lat = static_cast<const uint16_t*>(q_lat);
+    vp.q_rope = static_cast<const uint16_t*>(q_rope);
+    vp.block_table = block_table;
+    vp.seq_lens = seq_lens;
+    vp.n_tree = n_tree;
+    vp.q_off = q_off;
+    vp.anc = anc;
+    vp.req_state = req_state;
+    vp.items = items;
+    vp.item_count = item_count;
+    vp.status = status;
+    vp.out = out;
+    vp.lse = lse;
+    vp.part_out = part_out;
+    vp.part_lse = part_lse;
+    vp.batch = batch;
+    vp.total_q = total_q;
+    vp.page_size = page_size;
+    vp.max_pages = max_pages_per_seq;
+    vp.num_pages = num_pages;
+    vp.num_splits = splits;
+    vp.max_items = lay.max_items;
+    vp.scale_log2 = scale * 1.4426950408889634f;
+    vp.timeout_ns = kDefaultTimeoutNs;
+    const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
+    if (g_prof_begin && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    mla::mla_verify_kernel<<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (g_prof_end && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
+
+    // ---- merge of the split partials ----
+    if (splits > 1)
+        return launch_combine(part_out, part_lse, splits, static_cast<long long>(total_q) * MLA_NUM_HEADS, out, lse,
+                              stream);
+    return MLA_OK;
+}
+
+int mla_split_combine(const float* part_out, const float* part_lse, int num_splits, int rows, float* out, float* lse,
+                      cudaStream_t stream) {
+    if (num_splits < 1 || num_splits > MLA_MAX_SPLITS || rows < 0) return MLA_ERR_INVALID_ARG;
+    if (rows == 0) return MLA_OK;
+    if (!part_out || !part_lse || !out || !lse) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(part_out) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    return launch_combine(part_out, part_lse, num_splits, rows, out, lse, stream);
+}
+
+int mla_set_profile_events(cudaEvent_t begin, cudaEvent_t end) {
+    if ((begin == nullptr) != (end == nullptr)) return MLA_ERR_INVALID_ARG;
+    g_prof_begin = begin;
+    g_prof_end = end;
+    return MLA_OK;
+}
+
+int mla_read_status(const void* workspace, int* device_status) {
+    if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    *device_status = v;
+    return MLA_OK;
+}
+
+}  // extern "C"

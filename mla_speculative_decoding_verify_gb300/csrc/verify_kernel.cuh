@@ -1,0 +1,544 @@
+// Fused tree-verify MLA attention kernel for sm_103a.
+//
+// One 2-CTA cluster computes 128 output rows (2 tree tokens x 64 heads) of one
+// request over one KV split.  The pair divides the work along the feature
+// axis: CTA c owns latent dims [256c, 256c+256) and rope dims [32c, 32c+32).
+//   - QK^T: each CTA multiplies its half of q by its half of every key
+//     (tcgen05, q latent half resident in TMEM, keys streamed by TMA), giving
+//     a partial score tile; the partials are exchanged through distributed
+//     shared memory and added, so both CTAs hold the same full 576-dim score.
+//   - softmax: online and lazy (page "The Shared Memory Ceiling", section
+//     "Technical Deep Dive": running max and normaliser, earlier accumulators
+//     rescaled when the max grows), one thread per row, tree mask applied from
+//     the ancestor bit set of the row's node.
+//   - PV: each CTA accumulates its 256 columns of O = P * c_kv in TMEM (V is
+//     the c_kv latent, so the same shared-memory tile that served as K feeds
+//     PV).  P goes to TMEM as bf16; when a tile carries a large share of a
+//     row's mass a second bf16 "low part" of P is added so the result keeps
+//     close to fp32 weights.
+// TMEM: O [0,256) | q latent half [256,384) | S/P buffers [384,448), [448,512).
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+constexpr int kHeads = 64;
+constexpr int kDLatent = 512;
+constexpr int kDRope = 64;
+constexpr int kDqk = kDLatent + kDRope;
+constexpr int kBlockN = 64;            // keys per KV tile
+constexpr int kRows = 128;             // (token, head) rows per CTA
+constexpr int kTokensPerTile = kRows / kHeads;
+constexpr int kDLatentHalf = kDLatent / 2;
+constexpr int kDRopeHalf = kDRope / 2;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kChunkBytes = kBlockN * 64 * 2;          // [64 keys][64 dims] bf16, 128B swizzle
+constexpr uint32_t kRopeTileBytes = kBlockN * kDRopeHalf * 2;  // [64 keys][32 dims], 64B swizzle
+constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeTileBytes;
+constexpr uint32_t kQRopeBytes = kRows * kDRopeHalf * 2;
+constexpr uint32_t kXBufBytes = kRows * kBlockN * 4;       // one partial score tile, fp32
+constexpr uint32_t kOffStages = 0;
+constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
+constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;
+constexpr uint32_t kOffCtrl = kOffXBuf + 2 * kXBufBytes;
+constexpr uint32_t kCtrlBytes = 512;
+constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + slack for 1 KB alignment
+static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B swizzle");
+static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0, "region alignment");
+static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // S buffer x at kTmS + 64 * x
+
+constexpr float kLazyRescaleLog2 = 8.0f;   // rescale only when the max grows by > 2^8
+constexpr float kLowPartShare = 1.0f / 16.0f;
+
+// Status bits (1 << mla_status code).
+constexpr int kStatusTimeout = 1 << 5;
+constexpr int kStatusBadTree = 1 << 6;
+constexpr int kStatusBadBlock = 1 << 7;
+
+struct VerifyParams {
+    const uint16_t* q_lat;      // [total_q, 64, 512]
+    const uint16_t* q_rope;     // [total_q, 64, 64]
+    const int32_t* block_table; // [batch, max_pages]
+    const int32_t* seq_lens;    // [batch]
+    const int32_t* n_tree;      // [batch]
+    const int32_t* q_off;       // [batch + 1]   from the prep kernel
+    const uint64_t* anc;        // [total_q]     ancestor-or-self bit set of each node
+    const int32_t* req_state;   // [batch]       0 ok, 1 invalid (rows zeroed)
+    const int2* items;          // [max_items]   (request, row tile)
+    const int32_t* item_count;  // [1]
+    int* status;                // [1]
+    float* out;                 // [total_q, 64, 512]
+    float* lse;                 // [total_q, 64]
+    float* part_out;            // [num_splits, total_q * 64, 512]
+    float* part_lse;            // [num_splits, total_q * 64]
+    int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
+    float scale_log2;           // softmax scale * log2(e)
+    uint64_t timeout_ns;
+};
+
+struct Ctrl {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t kv_fixed[kStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t x_full[2];
+    uint64_t x_empty[2];
+    uint64_t q_ready;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int lo_flag[2];
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+
+__device__ __forceinline__ void raise_status(int* status, int bit) { atomicOr(status, bit); }
+
+// Which KV tiles [t0, t1) split `s` of `S` covers, for a request of n tiles.
+__device__ __forceinline__ void split_range(int n, int s, int S, int& t0, int& t1) {
+    t0 = static_cast<int>((static_cast<long long>(n) * s) / S);
+    t1 = static_cast<int>((static_cast<long long>(n) * (s + 1)) / S);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap map_lat,
+                  const __grid_constant__ CUtensorMap map_rope) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kOffCtrl);
+
+    const uint32_t c = cluster_ctarank();
+    const uint32_t peer = c ^ 1u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int item_slot = blockIdx.x >> 1;
+    const int split = blockIdx.y;
+
+    // ---- work item (identical in both CTAs of the pair) ----
+    if (item_slot >= __ldg(p.item_count)) return;
+    const int2 item = p.items[item_slot];
+    const int b = item.x;
+    const int tile = item.y;
+    const int T = __ldg(p.n_tree + b);
+    const int L = __ldg(p.seq_lens + b);
+    const int P = L - T;
+    const int qbase = __ldg(p.q_off + b) + kTokensPerTile * tile;
+    const int ntok = min(kTokensPerTile, T - kTokensPerTile * tile);
+    const bool bad = __ldg(p.req_state + b) != 0;
+    const int n_kv_tiles = bad ? 0 : (L + kBlockN - 1) / kBlockN;
+    int t0, t1;
+    split_range(n_kv_tiles, split, p.num_splits, t0, t1);
+    const int n = t1 - t0;
+
+    // rows of this thread (softmax warps only)
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int tok_local = r / kHeads;
+    const int head = r % kHeads;
+    const bool row_valid = warp >= 2 && tok_local < ntok;
+    const int qidx = qbase + tok_local;
+    const long long grow = static_cast<long long>(qidx) * kHeads + head;  // global output row
+
+    if (n <= 0) {
+        // Empty split or invalid request: normalised output 0, lse -inf.
+        if (row_valid) {
+            float* dst = (p.num_splits == 1)
+                             ? p.out + grow * kDLatent + kDLatentHalf * c
+                             : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
+                                   kDLatentHalf * c;
+            for (int d = 0; d < kDLatentHalf; d += 4)
+                *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c == 0) {
+                if (p.num_splits == 1) p.lse[grow] = -INFINITY;
+                else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    // ---- set-up ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->kv_full[s], 1);
+            mbar_init(&ctl->kv_empty[s], 1);
+            mbar_init(&ctl->kv_fixed[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&ctl->s_full[x], 1);
+            mbar_init(&ctl->p_full[x], kSoftmaxThreads);
+            mbar_init(&ctl->pv_done[x], 1);
+            mbar_init(&ctl->x_full[x], kSoftmaxThreads);
+            mbar_init(&ctl->x_empty[x], kSoftmaxThreads);
+            ctl->lo_flag[x] = 0;
+        }
+        mbar_init(&ctl->q_ready, kSoftmaxThreads);
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        fence_mbar_init_cluster();
+    }
+    if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_lat);
+        tma_prefetch_desc(&map_rope);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    cluster_sync();  // the peer's barriers are initialised before any remote arrive
+
+    volatile int* abort_flag = &ctl->abort;
+    const uint64_t lim = p.timeout_ns;
+    const uint32_t stage0 = smem_u32(smem + kOffStages);
+    const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        const uint64_t policy = l2_policy_evict_last();
+        bool ok = true;
+        int issued = 0;
+        for (int jj = 0; jj < n && ok; ++jj) {
+            const int st = jj % kStages;
+            if (jj >= kStages) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
+                if (!ok) break;
+            }
+            const int kpos = (t0 + jj) * kBlockN;
+            if (lane == 0) {
+                const int page_idx = kpos / p.page_size;
+                const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + page_idx);
+                if (page < 0 || page >= p.num_pages) raise_status(p.status, kStatusBadBlock);
+                // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
+                const int row = page * p.page_size + (kpos % p.page_size);
+                uint8_t* dst = smem + kOffStages + st * kStageBytes;
+                mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
+                for (int ch = 0; ch < 4; ++ch)
+                    tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
+                                kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
+                tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
+                            kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
+            }
+            ++issued;
+            __syncwarp();
+            if (kpos + kBlockN > L) {
+                // Last, partial tile: zero the rows past seq_len so that masked
+                // keys multiply finite values in PV.
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim));
+                if (!ok) break;
+                const int kvalid = L - kpos;
+                uint8_t* base = smem + kOffStages + st * kStageBytes;
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
+                    const int u = lane % 8;  // 16-byte unit of the row
+                    for (int ch = 0; ch < 4; ++ch)
+                        *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
+                    if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
+        }
+        // Do not leave the CTA with bulk copies in flight.
+        const int zero = 0;
+        for (int st = 0; st < kStages && st < issued; ++st) {
+            const int last = st + ((issued - 1 - st) / kStages) * kStages;  // last tile issued into stage st
+            mbar_wait(&ctl->kv_full[st], (last / kStages) & 1, &zero, lim);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
+        const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, 0, abort_flag, lim));
+        tc_fence_after();
+
+        auto issue_pv = [&](int i) -> bool {
+            const int x = i & 1;
+            const int st = i % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (i >> 1) & 1, abort_flag, lim))) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
+                const uint32_t sb = stage0 + st * kStageBytes;
+                const uint32_t pcol = tmem + kTmS + 64 * x;
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint64_t bdesc = smem_desc(sb + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+                    mma_ts(tmem + kTmO, pcol + 8 * kk, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (lo) {
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc(sb + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+                        mma_ts(tmem + kTmO, pcol + 32 + 8 * kk, bdesc, idesc_pv, 1u);
+                    }
+                }
+                mma_commit(&ctl->pv_done[x]);
+                mma_commit(&ctl->kv_empty[st]);
+            }
+            __syncwarp();
+            return true;
+        };
+
+        for (int jj = 0; jj < n && ok; ++jj) {
+            const int st = jj % kStages;
+            const int x = jj & 1;
+            const bool tail = (t0 + jj) * kBlockN + kBlockN > L;
+            ok = tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
+                      : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
+            if (ok && jj >= 2) ok = mbar_wait(&ctl->pv_done[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sb = stage0 + st * kStageBytes;
+                const uint32_t dS = tmem + kTmS + 64 * x;
+                for (int k = 0; k < kDLatentHalf / 16; ++k) {
+                    const uint64_t bdesc =
+                        smem_desc(sb + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_ts(dS, tmem + kTmQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+                }
+                for (int k = 0; k < kDRopeHalf / 16; ++k) {
+                    const uint64_t adesc = smem_desc(qrope_addr + k * 32, 16, 512, kSwizzle64B);
+                    const uint64_t bdesc = smem_desc(sb + 4 * kChunkBytes + k * 32, 16, 512, kSwizzle64B);
+                    mma_ss(dS, adesc, bdesc, idesc_qk, 1u);
+                }
+                mma_commit(&ctl->s_full[x]);
+            }
+            __syncwarp();
+            if (jj >= 1) ok = issue_pv(jj - 1);
+        }
+        if (ok) ok = issue_pv(n - 1);
+        if (!ok) {
+            if (lane == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
+        }
+        // Wait until every MMA issued by this CTA has finished before TMEM is released.
+        const int zero = 0;
+        if (lane == 0) mma_commit(&ctl->drain);
+        __syncwarp();
+        mbar_wait(&ctl->drain, 0, &zero, lim);
+    } else {
+        // ================= softmax / epilogue (thread = row) =================
+        const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+        const uint32_t trow = tmem + lane_base;
+        // q latent half -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory.
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + grow * kDLatent + kDLatentHalf * c);
+            for (int part = 0; part < 4; ++part) {
+                uint32_t v[32];
+                for (int u = 0; u < 8; ++u) {
+                    uint4 w = row_valid ? __ldg(src + part * 8 + u) : make_uint4(0, 0, 0, 0);
+                    v[4 * u + 0] = w.x;
+                    v[4 * u + 1] = w.y;
+                    v[4 * u + 2] = w.z;
+                    v[4 * u + 3] = w.w;
+                }
+                tmem_st32(trow + kTmQ + 32 * part, v);
+            }
+            const uint4* rs = reinterpret_cast<const uint4*>(p.q_rope + grow * kDRope + kDRopeHalf * c);
+            for (int u = 0; u < 4; ++u) {
+                uint4 w = row_valid ? __ldg(rs + u) : make_uint4(0, 0, 0, 0);
+                const uint32_t off = r * 64 + ((u ^ ((r >> 1) & 3)) << 4);
+                *reinterpret_cast<uint4*>(smem + kOffQRope + off) = w;
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&ctl->q_ready);
+        }
+
+        const int node = kTokensPerTile * tile + tok_local;
+        const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
+        const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
+        const uint32_t xbuf_peer = mapa(xbuf_local, peer);
+        float m_use = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        (void)node;
+
+        for (int jj = 0; jj < n; ++jj) {
+            const int x = jj & 1;
+            const uint32_t ph = (jj >> 1) & 1;
+            // Every wait result is made warp-uniform (tcgen05.ld/st are warp-collective)
+            // and, before the named barrier below, uniform over the 128 softmax threads.
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], ph, abort_flag, lim));
+            float s[kBlockN];
+            if (ok) {
+                tc_fence_after();
+                uint32_t a[32], bb[32];
+                tmem_ld32(trow + kTmS + 64 * x, a);
+                tmem_ld32(trow + kTmS + 64 * x + 32, bb);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    s[k] = __uint_as_float(a[k]);
+                    s[32 + k] = __uint_as_float(bb[k]);
+                }
+            }
+            // ---- exchange partial scores with the peer CTA ----
+            if (ok && jj >= 2) ok = mbar_wait<true>(&ctl->x_empty[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
+            if (ok) {
+                const uint32_t rowbase = xbuf_peer + x * kXBufBytes + r * (kBlockN * 4);
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    st_cluster_v4(rowbase + ((u ^ (r & 7)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2],
+                                  s[4 * u + 3]);
+                mbar_arrive_remote(&ctl->x_full[x], peer);
+                ok = mbar_wait<true>(&ctl->x_full[x], ph, abort_flag, lim);
+            }
+            if (ok) {
+                const uint32_t rowbase = xbuf_local + x * kXBufBytes + r * (kBlockN * 4);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float4 v = ld_shared_v4(rowbase + ((u ^ (r & 7)) << 4));
+                    s[4 * u] += v.x;
+                    s[4 * u + 1] += v.y;
+                    s[4 * u + 2] += v.z;
+                    s[4 * u + 3] += v.w;
+                }
+                mbar_arrive_remote(&ctl->x_empty[x], peer);
+            }
+            // ---- scale, tree mask ----
+            const int kpos = (t0 + jj) * kBlockN;
+            float mt = -INFINITY;
+            if (kpos + kBlockN <= P) {
+#pragma unroll
+                for (int k = 0; k < kBlockN; ++k) {
+                    s[k] *= p.scale_log2;
+                    mt = fmaxf(mt, s[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kBlockN; ++k) {
+                    const int t = kpos + k;
+                    bool vis = t < P;
+                    if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
+                    s[k] = vis ? s[k] * p.scale_log2 : -INFINITY;
+                    mt = fmaxf(mt, s[k]);
+                }
+            }
+            // ---- lazy online-softmax rescale (warp-uniform TMEM traffic) ----
+            const bool grow_max = ok && mt > m_use + kLazyRescaleLog2;
+            float alpha = 1.f;
+            if (grow_max) {
+                alpha = ex2_approx(m_use - mt);  // 0 when m_use is -inf
+                m_use = mt;
+                l *= alpha;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok && jj > 0 && __any_sync(0xffffffffu, grow_max)) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1,
+                                                       abort_flag, lim));
+                if (ok) {
+                    tc_fence_after();
+                    for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + kTmO + 32 * part, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st32(trow + kTmO + 32 * part, o);
+                    }
+                }
+            }
+            // all 128 softmax threads leave together or not at all
+            if (named_bar_or(1, kSoftmaxThreads, !ok)) {
+                ok = false;
+                break;
+            }
+            // ---- probabilities ----
+            float psum = 0.f, pmax = 0.f;
+            const bool live = m_use != -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kBlockN; ++k) {
+                s[k] = live ? ex2_approx(s[k] - m_use) : 0.f;
+                psum += s[k];
+                pmax = fmaxf(pmax, s[k]);
+            }
+            const bool vote = pmax > kLowPartShare * (l + psum);
+            const bool need_lo = named_bar_or(2, kSoftmaxThreads, vote);
+            uint32_t hi[32];
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+                const float h0 = bf16lo_to_f32(hi[k]);
+                const float h1 = bf16hi_to_f32(hi[k]);
+                s[2 * k] -= h0;
+                s[2 * k + 1] -= h1;
+                acc += h0 + h1;
+            }
+            tmem_st32(trow + kTmS + 64 * x, hi);
+            if (need_lo) {
+                uint32_t lo[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    lo[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+                    acc += bf16lo_to_f32(lo[k]) + bf16hi_to_f32(lo[k]);
+                }
+                tmem_st32(trow + kTmS + 64 * x + 32, lo);
+            }
+            tmem_wait_st();
+            l += acc;
+            if (r == 0) ctl->lo_flag[x] = need_lo ? 1 : 0;
+            tc_fence_before();
+            mbar_arrive(&ctl->p_full[x]);
+        }
+
+        // ---- epilogue ----
+        if (ok) ok = mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, lim);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (r == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
+        } else {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            float* dst = (p.num_splits == 1)
+                             ? p.out + grow * kDLatent + kDLatentHalf * c
+                             : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
+                                   kDLatentHalf * c;
+            for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                uint32_t o[32];
+                tmem_ld32(trow + kTmO + 32 * part, o);
+                tmem_wait_ld();
+                if (row_valid) {
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<float4*>(dst + 32 * part + 4 * u) =
+                            make_float4(__uint_as_float(o[4 * u]) * inv_l, __uint_as_float(o[4 * u + 1]) * inv_l,
+                                        __uint_as_float(o[4 * u + 2]) * inv_l, __uint_as_float(o[4 * u + 3]) * inv_l);
+                }
+            }
+            if (row_valid && c == 0) {
+                const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
+                const float v = lse2 * 0.6931471805599453f;
+                if (p.num_splits == 1) p.lse[grow] = v;
+                else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = v;
+            }
+        }
+    }
+
+    // ---- tear-down ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    cluster_sync();  // the peer may still be writing to this CTA's shared memory until here
+}
+
+}  // namespace mla

@@ -1,0 +1,65 @@
+"""Work and traffic counts of a verify batch (for throughput and roofline figures).
+
+Algorithmic work is what the method must do, not what a dense kernel would:
+per (row, visible key) 2*576 flops for q.k and 2*512 for p*v; masked tree
+pairs are not counted.  KV bytes count each request's rows once (logical) or
+each physical page once (unique; shared prefix pages counted once).
+"""
+from __future__ import annotations
+
+import hashlib
+import os
+
+import numpy as np
+
+FLOPS_PER_ROW_KEY = 2 * (512 + 64) + 2 * 512
+KV_ROW_BYTES = (512 + 64) * 2
+
+
+def visible_tree_pairs(parent: np.ndarray) -> int:
+    """Number of (node, ancestor-or-self) pairs of one draft tree."""
+    depth = np.zeros(len(parent), dtype=np.int64)
+    for i, p in enumerate(parent):
+        depth[i] = 1 + (depth[p] if p >= 0 else 0)
+    return int(depth.sum())
+
+
+def algorithmic_flops(inp) -> int:
+    total = 0
+    off = 0
+    for b in range(inp.batch):
+        T = int(inp.n_tree[b])
+        P = int(inp.seq_lens[b]) - T
+        total += inp.num_heads * FLOPS_PER_ROW_KEY * (T * P + visible_tree_pairs(inp.tree_parent[off:off + T]))
+        off += T
+    return int(total)
+
+
+def kv_bytes(inp, unique: bool = False) -> int:
+    if not unique:
+        return int(inp.seq_lens.astype(np.int64).sum()) * KV_ROW_BYTES
+    pages = set()
+    for b in range(inp.batch):
+        n = (int(inp.seq_lens[b]) + inp.page_size - 1) // inp.page_size
+        pages.update(int(p) for p in inp.block_table[b, :n])
+    return len(pages) * inp.page_size * KV_ROW_BYTES
+
+
+def io_bytes(inp) -> dict:
+    """Bytes of the call's inputs (host -> device) and outputs (device -> host)."""
+    inputs = sum(a.nbytes for a in (inp.q_lat, inp.q_rope, inp.kv_cache, inp.block_table,
+                                    inp.seq_lens, inp.tree_parent, inp.n_tree))
+    outputs = inp.total_q * inp.num_heads * (512 + 1) * 4
+    return {"h2d": int(inputs), "d2h": int(outputs)}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; profile figures taken on other sources are stale."""
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(here)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(here, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]

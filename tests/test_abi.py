@@ -1,0 +1,86 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared entry
+point, and rejects bad scalar arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_speculative_decoding_verify_gb300 import binding
+from mla_speculative_decoding_verify_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla_verify.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return binding.lib()
+
+
+def test_header_declares_the_binding_surface():
+    assert sorted(binding.EXPORTED) == declared_functions()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_error_strings(lib):
+    assert binding.version() >= 100
+    for code in range(0, 9):
+        assert binding.error_string(code) not in ("", "unknown status")
+    assert binding.error_string(99) == "unknown status"
+
+
+def _call(**over):
+    args = dict(q_lat=16, q_rope=16, kv_cache=16, block_table=16, seq_lens=16, tree_parent=16,
+                n_tree=16, scale=0.07, out=16, lse=16, stream=None, batch=1, total_q=1, max_tree=1,
+                max_seq_len=65, num_heads=64, page_size=64, num_pages=2, max_pages_per_seq=2,
+                num_splits=0, workspace=256, workspace_bytes=1 << 20)
+    args.update(over)
+    return binding.verify_attn(**args)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_heads=32), binding.MLA_ERR_UNSUPPORTED),
+    (dict(page_size=48), binding.MLA_ERR_UNSUPPORTED),
+    (dict(page_size=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(max_tree=65), binding.MLA_ERR_UNSUPPORTED),
+    (dict(num_splits=65), binding.MLA_ERR_UNSUPPORTED),
+    (dict(batch=-1), binding.MLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.MLA_ERR_INVALID_ARG),
+    (dict(q_lat=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(out=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(kv_cache=24), binding.MLA_ERR_INVALID_ARG),   # not 16-byte aligned
+    (dict(num_pages=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(batch=0, total_q=0), binding.MLA_OK),           # nothing to do
+])
+def test_host_argument_checks(lib, over, code):
+    assert _call(**over) == code
+
+
+def test_combine_argument_checks(lib):
+    assert binding.split_combine(16, 16, 0, 4, 16, 16, None) == binding.MLA_ERR_INVALID_ARG
+    assert binding.split_combine(16, 16, 65, 4, 16, 16, None) == binding.MLA_ERR_INVALID_ARG
+    assert binding.split_combine(None, 16, 2, 4, 16, 16, None) == binding.MLA_ERR_INVALID_ARG
+    assert binding.split_combine(16, 16, 2, 0, 16, 16, None) == binding.MLA_OK
+
+
+def test_split_heuristic_and_workspace(lib):
+    assert binding.num_splits(4, 64, 16, 4112, requested=5) == 5
+    assert binding.num_splits(4, 64, 16, 4112, requested=500) == binding.MAX_SPLITS
+    s = binding.num_splits(2, 128, 64, 65600)
+    assert 1 <= s <= binding.MAX_SPLITS
+    w1 = binding.workspace_size(16, 512, 32, 16416, splits=1)
+    w4 = binding.workspace_size(16, 512, 32, 16416, splits=4)
+    assert w4 - w1 >= 4 * 512 * 64 * 512 * 4
+    assert binding.workspace_size(1, 1, 1, 1, num_heads=32) == 0

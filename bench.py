@@ -233,6 +233,9 @@ def run_ours(args, ranks: Ranks):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:           # torch creates the CUDA events lazily, on first record
+        a.record(stream)
+        b.record(stream)
     clocks = ClockSampler(ranks.local)
     clocks.start()
     time.sleep(0.3)

@@ -151,6 +151,35 @@ int mla_split_combine(const float *part_out, const float *part_lse, int num_spli
                       float *out, float *lse, cudaStream_t stream);
 
 /*
+ * mla_verify_attn for callers that cannot allocate device memory: the page
+ * text has no counterpart to this entry point.  Some callers cannot provide a
+ * workspace -- e.g. a plugin inside a serving engine that owns all device
+ * memory through its own pool and exposes no workspace hook, or a
+ * latency-critical loop where cudaMalloc (which may synchronise the device)
+ * is not acceptable.  This variant keeps the per-call scratch (status word,
+ * query offsets, ancestor bit sets, work list) in a 1 MiB static device array
+ * that every GPU loading the library holds until the process exits, and runs
+ * with a single KV split.  The caller still passes inputs and outputs; the
+ * arguments mean what they mean for mla_verify_attn.  It allocates nothing.
+ *  - Sizes whose scratch would exceed 1 MiB (roughly 12 B per tree token plus
+ *    20 B per request) return MLA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address; make that
+ *    first call before any stream capture on that device.
+ *  - All calls share the array.  The kernels clear what must start at zero and
+ *    overwrite the rest before reading it, so a call never sees an earlier
+ *    call's data, but calls whose work overlaps on the GPU (other streams,
+ *    other host threads) race on it and must be serialised by the caller.
+ *  - The device status word is not readable for this variant; rows of a
+ *    request with invalid data are still written as out = 0, lse = -inf.
+ */
+int mla_verify_attn_noalloc(const void *q_lat, const void *q_rope, const void *kv_cache,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const int32_t *tree_parent, const int32_t *n_tree, float scale,
+                            float *out, float *lse, cudaStream_t stream,
+                            int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
+                            int page_size, int num_pages, int max_pages_per_seq);
+
+/*
  * Measurement hook: while set, every mla_verify_attn call records `begin`
  * immediately before and `end` immediately after the launch of its fused
  * verify kernel, on the call's stream, so the kernel can be timed alone.

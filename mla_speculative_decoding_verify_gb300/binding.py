@@ -33,7 +33,7 @@ MAX_SPLITS = 64
 
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
-            "mla_read_status", "mla_set_profile_events")
+            "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
         L.mla_verify_attn.restype = i32
         L.mla_verify_attn.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                       i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz]
+        L.mla_verify_attn_noalloc.restype = i32
+        L.mla_verify_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                              i32, i32, i32, i32, i32, i32, i32, i32]
         L.mla_split_combine.restype = i32
         L.mla_split_combine.argtypes = [vp, vp, i32, i32, vp, vp, vp]
         L.mla_set_profile_events.restype = i32
@@ -116,6 +119,17 @@ def verify_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_t
                                      n_tree, float(scale), out, lse, stream, batch, total_q,
                                      max_tree, max_seq_len, num_heads, page_size, num_pages,
                                      max_pages_per_seq, num_splits, workspace, workspace_bytes))
+
+
+def verify_attn_noalloc(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree,
+                        scale, out, lse, stream, batch, total_q, max_tree, max_seq_len, num_heads,
+                        page_size, num_pages, max_pages_per_seq) -> int:
+    """Raw call of the allocation-free entry point (static 1 MiB device scratch,
+    one KV split) for callers that cannot provide a workspace; returns the status."""
+    return int(lib().mla_verify_attn_noalloc(q_lat, q_rope, kv_cache, block_table, seq_lens,
+                                             tree_parent, n_tree, float(scale), out, lse, stream,
+                                             batch, total_q, max_tree, max_seq_len, num_heads,
+                                             page_size, num_pages, max_pages_per_seq))
 
 
 def split_combine(part_out, part_lse, num_splits, rows, out, lse, stream) -> int:

@@ -9,6 +9,7 @@ import sys
 _HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(_HERE)
 SRC = os.path.join(_HERE, "csrc", "mla_verify.cu")
+SRC_NOALLOC = os.path.join(_HERE, "csrc", "mla_verify_noalloc.cu")
 HEADERS = [os.path.join(_HERE, "csrc", f) for f in os.listdir(os.path.join(_HERE, "csrc"))
            if f.endswith((".cuh", ".h"))] + [os.path.join(ROOT, "include", "mla_verify.h")]
 OUT = os.path.join(_HERE, "libmla_verify.so")
@@ -26,7 +27,7 @@ def up_to_date() -> bool:
     if not os.path.exists(OUT):
         return False
     t = os.path.getmtime(OUT)
-    return all(os.path.getmtime(f) <= t for f in [SRC] + HEADERS)
+    return all(os.path.getmtime(f) <= t for f in [SRC, SRC_NOALLOC] + HEADERS)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -34,7 +35,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return OUT
     tmp = OUT + f".tmp{os.getpid()}"
     cmd = [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-           "-I", os.path.join(ROOT, "include"), SRC, "-o", tmp]
+           "-I", os.path.join(ROOT, "include"), SRC, SRC_NOALLOC, "-o", tmp]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)

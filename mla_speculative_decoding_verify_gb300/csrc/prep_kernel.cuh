@@ -1,7 +1,9 @@
 // Per-call metadata for the verify kernel: query offsets of the requests,
 // the ancestor-or-self bit set of every draft-tree node, input validation
 // into the status word, and the list of (request, row tile) work items in
-// longest-request-first order.  One thread block; integer work only.
+// longest-request-first order.  One thread block; integer work only.  Each
+// request is handled by one warp (its tree fits in two words per lane), so
+// no thread walks a long chain of dependent global loads.
 #pragma once
 
 #include <cstdint>
@@ -11,8 +13,9 @@
 namespace mla {
 
 constexpr int kPrepThreads = 1024;
+constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kLptMaxBatch = 1024;  // above this the items keep request order
-constexpr int kMaxTree = 64;         // the ancestor bit set is one 64-bit word
+constexpr int kMaxTree = 64;        // the ancestor bit set is one 64-bit word
 
 struct PrepParams {
     const int32_t* block_table;  // [batch, max_pages]
@@ -21,7 +24,7 @@ struct PrepParams {
     const int32_t* n_tree;       // [batch]
     int32_t* q_off;              // [batch + 1]
     int32_t* req_state;          // [batch]
-    int32_t* order;              // [batch]  scratch: requests by descending length
+    int32_t* order;              // [batch]      scratch: requests by descending length
     int32_t* item_off;           // [batch + 1]  scratch: first item of each request
     uint64_t* anc;               // [total_q]
     int2* items;                 // [max_items]
@@ -67,7 +70,10 @@ __device__ void block_exclusive_scan(int n, F f, int32_t* dst, int32_t* warp_sum
 
 __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepParams p) {
     __shared__ int32_t warp_sums[32];
+    __shared__ int32_t tree_par[kPrepWarps][kMaxTree];
+    __shared__ uint64_t tree_anc[kPrepWarps][kMaxTree];
     const int tid = threadIdx.x;
+    const int lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
         *p.status = 0;
         *p.item_count = 0;
@@ -78,65 +84,81 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     block_exclusive_scan(p.batch, [&](int b) { return p.n_tree[b]; }, p.q_off, warp_sums);
     if (tid == 0 && p.q_off[p.batch] != p.total_q) atomicOr(p.status, kStatusBadTree);
 
-    // 2. validate each request: sizes, parents, block ids
-    for (int b = tid; b < p.batch; b += kPrepThreads) {
+    // 2. one warp per request: validate sizes, parents and block ids, then the
+    //    ancestor bit sets by pointer jumping (6 rounds cover depth 64)
+    for (int b = wid; b < p.batch; b += kPrepWarps) {
         const int T = p.n_tree[b];
         const int L = p.seq_lens[b];
-        int state = 0;
-        int bits = 0;
-        if (T < 0 || T > kMaxTree || L < T || p.q_off[b] + T > p.total_q ||
-            p.q_off[b] < 0) {
-            state = 2;  // outputs of this request are not written at all
-            bits |= kStatusBadTree;
-        } else {
-            for (int i = 0; i < T; ++i) {
-                const int par = p.tree_parent[p.q_off[b] + i];
-                if (par < -1 || par >= i) {
-                    state = 1;
-                    bits |= kStatusBadTree;
-                }
+        const int base = p.q_off[b];
+        const bool shape_ok = T >= 0 && T <= kMaxTree && L >= T && base >= 0 && base + T <= p.total_q;
+        bool bad_parent = false, bad_block = false;
+        if (shape_ok) {
+            for (int i = lane; i < T; i += 32) {
+                const int par = p.tree_parent[base + i];
+                const bool good = par >= -1 && par < i;
+                tree_par[wid][i] = good ? par : -1;
+                bad_parent |= !good;
             }
             const int pages = (L + p.page_size - 1) / p.page_size;
             if (pages > p.max_pages) {
-                state = 1;
-                bits |= kStatusBadBlock;
+                bad_block = true;
             } else {
-                for (int k = 0; k < pages; ++k) {
-                    const int pg = p.block_table[static_cast<long long>(b) * p.max_pages + k];
-                    if (pg < 0 || pg >= p.num_pages) {
-                        state = 1;
-                        bits |= kStatusBadBlock;
-                        break;
-                    }
+                const int32_t* row = p.block_table + static_cast<long long>(b) * p.max_pages;
+                for (int k = lane; k < pages; k += 32) {
+                    const int pg = row[k];
+                    bad_block |= pg < 0 || pg >= p.num_pages;
                 }
             }
         }
-        p.req_state[b] = state;
-        if (bits) atomicOr(p.status, bits);
+        bad_parent = __any_sync(0xffffffffu, bad_parent);
+        bad_block = __any_sync(0xffffffffu, bad_block);
+        const bool all_ok = shape_ok && !bad_parent && !bad_block;
+        if (lane == 0) {
+            p.req_state[b] = shape_ok ? (all_ok ? 0 : 1) : 2;  // 2: outputs not written at all
+            const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0);
+            if (bits) atomicOr(p.status, bits);
+        }
+        __syncwarp();
+        if (shape_ok) {
+            // pointer jumping: anc(i) = {i} u anc(parent(i))
+            uint64_t a[2];
+            int up[2];
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                a[h] = i < T ? (1ull << i) : 0ull;
+                up[h] = i < T ? tree_par[wid][i] : -1;
+                if (i < T) tree_anc[wid][i] = a[h];
+            }
+            __syncwarp();
+            for (int round = 0; round < 6; ++round) {
+                uint64_t na[2];
+                int nu[2];
+                for (int h = 0; h < 2; ++h) {
+                    na[h] = a[h] | (up[h] >= 0 ? tree_anc[wid][up[h]] : 0ull);
+                    nu[h] = up[h] >= 0 ? tree_par[wid][up[h]] : -1;
+                }
+                __syncwarp();
+                for (int h = 0; h < 2; ++h) {
+                    const int i = lane + 32 * h;
+                    a[h] = na[h];
+                    up[h] = nu[h];
+                    if (i < T) {
+                        tree_anc[wid][i] = a[h];
+                        tree_par[wid][i] = up[h];
+                    }
+                }
+                __syncwarp();
+            }
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i < T) p.anc[base + i] = all_ok ? a[h] : 0ull;
+            }
+        }
+        __syncwarp();
     }
     __syncthreads();
 
-    // 3. ancestor-or-self bit sets, one node per thread (walk bounded by the tree size)
-    for (int q = tid; q < p.total_q; q += kPrepThreads) {
-        int lo = 0, hi = p.batch - 1;  // request owning q: last b with q_off[b] <= q
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.q_off[mid] <= q) lo = mid; else hi = mid - 1;
-        }
-        const int b = lo;
-        uint64_t bits = 0;
-        if (p.req_state[b] == 0) {
-            const int base = p.q_off[b];
-            int j = q - base;
-            for (int step = 0; j >= 0 && step < kMaxTree; ++step) {
-                bits |= 1ull << j;
-                j = p.tree_parent[base + j];
-            }
-        }
-        p.anc[q] = bits;
-    }
-
-    // 4. work items, longest requests first (better tail of the grid)
+    // 3. work items, longest requests first (better tail of the grid)
     const bool lpt = p.batch <= kLptMaxBatch;
     for (int b = tid; b < p.batch; b += kPrepThreads) {
         int rank = b;

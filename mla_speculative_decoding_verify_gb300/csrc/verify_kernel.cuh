@@ -35,7 +35,7 @@ constexpr int kRows = 128;             // (token, head) rows per CTA
 constexpr int kTokensPerTile = kRows / kHeads;
 constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kChunkBytes = kBlockN * 64 * 2;          // [64 keys][64 dims] bf16, 128B swizzle
@@ -45,12 +45,13 @@ constexpr uint32_t kQRopeBytes = kRows * kDRopeHalf * 2;
 constexpr uint32_t kXBufBytes = kRows * kBlockN * 4;       // one partial score tile, fp32
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;
-constexpr uint32_t kOffCtrl = kOffXBuf + 2 * kXBufBytes;
+constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;          // 2 receive buffers (peer's partials)
+constexpr uint32_t kOffStaging = kOffXBuf + 2 * kXBufBytes;     // own partial, source of the bulk copy
+constexpr uint32_t kOffCtrl = kOffStaging + kXBufBytes;
 constexpr uint32_t kCtrlBytes = 512;
 constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + slack for 1 KB alignment
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B swizzle");
-static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0, "region alignment");
+static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0, "region alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
 
 constexpr uint32_t kTmemCols = 512;
@@ -92,13 +93,15 @@ struct Ctrl {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t pv_done[2];
-    uint64_t x_full[2];
-    uint64_t x_empty[2];
+    uint64_t x_full[2];    // peer's partial for tile j landed in receive buffer j % 2 (bytes)
+    uint64_t x_empty[2];   // peer finished reading the partial this CTA sent into its buffer j % 2
+    uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
     uint64_t q_ready;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int lo_flag[2];
+    int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -177,13 +180,17 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             mbar_init(&ctl->s_full[x], 1);
             mbar_init(&ctl->p_full[x], kSoftmaxThreads);
             mbar_init(&ctl->pv_done[x], 1);
-            mbar_init(&ctl->x_full[x], kSoftmaxThreads);
-            mbar_init(&ctl->x_empty[x], kSoftmaxThreads);
+            mbar_init(&ctl->x_full[x], 1);
+            mbar_init(&ctl->x_empty[x], 1);
             ctl->lo_flag[x] = 0;
         }
+        for (int k = 0; k < 3; ++k) ctl->tile_flags[k] = 0;
         mbar_init(&ctl->q_ready, kSoftmaxThreads);
         mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->stg_free, 1);
         ctl->abort = 0;
+        // byte counts of the first two incoming partials, posted before the peer can send
+        for (int x = 0; x < 2 && x < n; ++x) mbar_arrive_expect_tx(&ctl->x_full[x], kXBufBytes);
         fence_mbar_init_cluster();
     }
     if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -364,6 +371,10 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
         const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
         const uint32_t xbuf_peer = mapa(xbuf_local, peer);
+        const uint32_t stg_local = smem_u32(smem + kOffStaging);
+        const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full[0]), peer);
+        int posted = n < 2 ? n : 2;  // incoming partials whose byte count is posted (thread r == 0)
+        int consumed = 0;            // incoming partials waited for (thread r == 0)
         float m_use = -INFINITY;
         float l = 0.f;
         bool ok = true;
@@ -372,8 +383,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         for (int jj = 0; jj < n; ++jj) {
             const int x = jj & 1;
             const uint32_t ph = (jj >> 1) & 1;
-            // Every wait result is made warp-uniform (tcgen05.ld/st are warp-collective)
-            // and, before the named barrier below, uniform over the 128 softmax threads.
+            // Wait outcomes are made warp-uniform (tcgen05.ld/st are warp-collective);
+            // the per-tile flag word below makes the stop decision uniform over all
+            // 128 softmax threads before they touch the next named barrier.
             ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], ph, abort_flag, lim));
             float s[kBlockN];
             if (ok) {
@@ -389,17 +401,27 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 }
             }
             // ---- exchange partial scores with the peer CTA ----
-            if (ok && jj >= 2) ok = mbar_wait<true>(&ctl->x_empty[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
+            // own partial -> staging (local) -> TMA bulk copy into the peer's receive
+            // buffer, bytes counted on the peer's x_full; then read the peer's partial.
+            if (ok && jj >= 1) ok = mbar_wait<true>(&ctl->stg_free, (jj - 1) & 1, abort_flag, lim);
             if (ok) {
-                const uint32_t rowbase = xbuf_peer + x * kXBufBytes + r * (kBlockN * 4);
+                const uint32_t rowbase = stg_local + r * (kBlockN * 4);
 #pragma unroll
                 for (int u = 0; u < 16; ++u)
-                    st_cluster_v4(rowbase + ((u ^ (r & 7)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2],
-                                  s[4 * u + 3]);
-                mbar_arrive_remote(&ctl->x_full[x], peer);
-                ok = mbar_wait<true>(&ctl->x_full[x], ph, abort_flag, lim);
+                    st_shared_v4(rowbase + ((u ^ (r & 7)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+                fence_proxy_async_smem();
             }
+            named_bar_sync(3, kSoftmaxThreads);
+            if (r == 0 && ok) {
+                if (jj >= 2) ok = mbar_wait<true>(&ctl->x_empty[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
+                if (ok) bulk_copy_to_peer(xbuf_peer + x * kXBufBytes, stg_local, kXBufBytes, xfull_peer + 8u * x);
+            }
+            if (ok) ok = mbar_wait<true>(&ctl->x_full[x], ph, abort_flag, lim);
             if (ok) {
+                if (r == 0) {
+                    ++consumed;
+                    mbar_arrive_remote_relaxed(&ctl->stg_free, peer);  // our staging landed: peer may reuse its own
+                }
                 const uint32_t rowbase = xbuf_local + x * kXBufBytes + r * (kBlockN * 4);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -409,7 +431,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     s[4 * u + 2] += v.z;
                     s[4 * u + 3] += v.w;
                 }
-                mbar_arrive_remote(&ctl->x_empty[x], peer);
             }
             // ---- scale, tree mask ----
             const int kpos = (t0 + jj) * kBlockN;
@@ -454,11 +475,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     }
                 }
             }
-            // all 128 softmax threads leave together or not at all
-            if (named_bar_or(1, kSoftmaxThreads, !ok)) {
-                ok = false;
-                break;
-            }
             // ---- probabilities ----
             float psum = 0.f, pmax = 0.f;
             const bool live = m_use != -INFINITY;
@@ -468,32 +484,46 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 psum += s[k];
                 pmax = fmaxf(pmax, s[k]);
             }
-            const bool vote = pmax > kLowPartShare * (l + psum);
-            const bool need_lo = named_bar_or(2, kSoftmaxThreads, vote);
+            // One named barrier decides, uniformly for the 128 threads, whether to stop
+            // (bit 1) and whether this tile needs the low part of P (bit 0).
+            volatile int* flags = &ctl->tile_flags[jj % 3];
+            const int mine = (ok ? 0 : 2) | ((pmax > kLowPartShare * (l + psum)) ? 1 : 0);
+            if (mine) atomicOr(const_cast<int*>(flags), mine);
+            named_bar_sync(1, kSoftmaxThreads);
+            const int tf = *flags;
+            if (tf & 2) {
+                ok = false;
+                break;
+            }
+            const bool need_lo = tf & 1;
+            if (r == 0) {
+                ctl->tile_flags[(jj + 2) % 3] = 0;  // read by everyone before this barrier; next used by tile jj + 2
+                if (jj + 2 < n) {
+                    mbar_arrive_expect_tx(&ctl->x_full[x], kXBufBytes);  // re-arm for tile jj + 2
+                    ++posted;
+                }
+                mbar_arrive_remote_relaxed(&ctl->x_empty[x], peer);  // receive buffer x read by all
+                ctl->lo_flag[x] = need_lo ? 1 : 0;
+            }
             uint32_t hi[32];
             float acc = 0.f;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-                const float h0 = bf16lo_to_f32(hi[k]);
-                const float h1 = bf16hi_to_f32(hi[k]);
-                s[2 * k] -= h0;
-                s[2 * k + 1] -= h1;
-                acc += h0 + h1;
+                acc += bf16lo_to_f32(hi[k]) + bf16hi_to_f32(hi[k]);
             }
             tmem_st32(trow + kTmS + 64 * x, hi);
             if (need_lo) {
                 uint32_t lo[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    lo[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
+                    lo[k] = pack_bf16x2(s[2 * k] - bf16lo_to_f32(hi[k]), s[2 * k + 1] - bf16hi_to_f32(hi[k]));
                     acc += bf16lo_to_f32(lo[k]) + bf16hi_to_f32(lo[k]);
                 }
                 tmem_st32(trow + kTmS + 64 * x + 32, lo);
             }
             tmem_wait_st();
             l += acc;
-            if (r == 0) ctl->lo_flag[x] = need_lo ? 1 : 0;
             tc_fence_before();
             mbar_arrive(&ctl->p_full[x]);
         }
@@ -502,7 +532,12 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         if (ok) ok = mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, lim);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
-            if (r == 0) raise_status(p.status, kStatusTimeout);
+            if (r == 0) {
+                raise_status(p.status, kStatusTimeout);
+                // do not leave while the peer's bulk copies may still land in this CTA
+                const int zero = 0;
+                for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full[t & 1], (t >> 1) & 1, &zero, lim);
+            }
             *abort_flag = 1;
         } else {
             tc_fence_after();

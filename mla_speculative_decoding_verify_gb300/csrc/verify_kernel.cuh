@@ -434,13 +434,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             }
             // ---- scale, tree mask ----
             const int kpos = (t0 + jj) * kBlockN;
-            float mt = -INFINITY;
             if (kpos + kBlockN <= P) {
 #pragma unroll
-                for (int k = 0; k < kBlockN; ++k) {
-                    s[k] *= p.scale_log2;
-                    mt = fmaxf(mt, s[k]);
-                }
+                for (int k = 0; k < kBlockN; ++k) s[k] *= p.scale_log2;
             } else {
 #pragma unroll
                 for (int k = 0; k < kBlockN; ++k) {
@@ -448,9 +444,16 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     bool vis = t < P;
                     if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
                     s[k] = vis ? s[k] * p.scale_log2 : -INFINITY;
-                    mt = fmaxf(mt, s[k]);
                 }
             }
+            // tree reductions (8 independent chains) keep the dependent latency short
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+            for (int k = 8; k < kBlockN; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             // ---- lazy online-softmax rescale (warp-uniform TMEM traffic) ----
             const bool grow_max = ok && mt > m_use + kLazyRescaleLog2;
             float alpha = 1.f;
@@ -476,14 +479,19 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 }
             }
             // ---- probabilities ----
-            float psum = 0.f, pmax = 0.f;
             const bool live = m_use != -INFINITY;
+            float ps[8], pm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ps[k] = pm[k] = 0.f;
 #pragma unroll
             for (int k = 0; k < kBlockN; ++k) {
                 s[k] = live ? ex2_approx(s[k] - m_use) : 0.f;
-                psum += s[k];
-                pmax = fmaxf(pmax, s[k]);
+                ps[k & 7] += s[k];
+                pm[k & 7] = fmaxf(pm[k & 7], s[k]);
             }
+            const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                     fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             // One named barrier decides, uniformly for the 128 threads, whether to stop
             // (bit 1) and whether this tile needs the low part of P (bit 0).
             volatile int* flags = &ctl->tile_flags[jj % 3];
@@ -506,11 +514,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 ctl->lo_flag[x] = need_lo ? 1 : 0;
             }
             uint32_t hi[32];
-            float acc = 0.f;
+            float ac[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ac[k] = 0.f;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-                acc += bf16lo_to_f32(hi[k]) + bf16hi_to_f32(hi[k]);
+                ac[k & 7] += bf16lo_to_f32(hi[k]) + bf16hi_to_f32(hi[k]);
             }
             tmem_st32(trow + kTmS + 64 * x, hi);
             if (need_lo) {
@@ -518,12 +528,12 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
                     lo[k] = pack_bf16x2(s[2 * k] - bf16lo_to_f32(hi[k]), s[2 * k + 1] - bf16hi_to_f32(hi[k]));
-                    acc += bf16lo_to_f32(lo[k]) + bf16hi_to_f32(lo[k]);
+                    ac[k & 7] += bf16lo_to_f32(lo[k]) + bf16hi_to_f32(lo[k]);
                 }
                 tmem_st32(trow + kTmS + 64 * x + 32, lo);
             }
             tmem_wait_st();
-            l += acc;
+            l += ((ac[0] + ac[1]) + (ac[2] + ac[3])) + ((ac[4] + ac[5]) + (ac[6] + ac[7]));
             tc_fence_before();
             mbar_arrive(&ctl->p_full[x]);
         }

@@ -171,3 +171,41 @@ def test_argument_errors_before_launch():
     with pytest.raises(binding.MlaError) as e:
         binding.verify(db, workspace=small)
     assert e.value.code == binding.MLA_ERR_WORKSPACE
+
+
+def test_cuda_graph_capture_and_replay():
+    """mla_verify_attn is capturable in a CUDA graph after mla_init: the graph
+    replays prep -> verify -> combine and reads the buffers at replay time."""
+    import torch
+    ensure_gpu()
+    kw = dict(tree_kind="uniform", stream=502)
+    a = I.make_inputs([700, 130, 64], [9, 33, 4], seed=11, **kw)
+    b = I.make_inputs([700, 130, 64], [9, 33, 4], seed=12, **kw)
+    assert a.kv_cache.shape == b.kv_cache.shape and a.block_table.shape == b.block_table.shape
+    db = binding.DeviceBatch(a, "cuda:0")
+    splits = 3
+    out = torch.empty((a.total_q, a.num_heads, 512), dtype=torch.float32, device="cuda:0")
+    lse = torch.empty((a.total_q, a.num_heads), dtype=torch.float32, device="cuda:0")
+    ws = torch.empty(binding.workspace_size(a.batch, a.total_q, a.max_tree, a.max_seq_len, a.num_heads,
+                                            splits), dtype=torch.uint8, device="cuda:0")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=torch.cuda.current_stream())
+    for tag, inp in (("second batch", b), ("first batch", a)):
+        for name in ("q_lat", "q_rope", "kv_cache", "block_table", "seq_lens", "tree_parent", "n_tree"):
+            src = torch.from_numpy(np.ascontiguousarray(getattr(inp, name)).view(
+                np.int32 if getattr(inp, name).dtype == np.int32 else np.int16))
+            getattr(db, name).copy_(src)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.read_status(ws.data_ptr()) == 0
+        ref_o, ref_l = oracle.verify(inp)
+        assert_close(out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                     ref_o, ref_l, f"graph replay, {tag}")

@@ -105,7 +105,8 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
  *              -1 for a root (child of the last prefix token); parent[i] < i
  *  n_tree      device int32 [batch]  tree tokens of each request; requests are
  *              laid out back to back in q_lat / tree_parent / out
- *  scale       softmax scale applied to q . k (latent and rope parts alike)
+ *  scale       softmax scale applied to q . k (latent and rope parts alike);
+ *              finite and > 0, else MLA_ERR_INVALID_ARG
  *  out         device fp32 [total_q, num_heads, 512]  softmax-weighted c_kv
  *  lse         device fp32 [total_q, num_heads]  natural-log log-sum-exp of the
  *              scaled scores over the visible keys

@@ -208,7 +208,7 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
                     int num_splits, void* workspace, size_t workspace_bytes) {
     // ---- host-checkable arguments ----
     if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
-        num_splits < 0 || page_size <= 0 || !std::isfinite(scale))
+        num_splits < 0 || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
         return MLA_ERR_INVALID_ARG;
     if (num_heads != MLA_NUM_HEADS || page_size % mla::kBlockN != 0 || max_tree > MLA_MAX_TREE ||
         num_splits > MLA_MAX_SPLITS)

@@ -316,6 +316,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// The descriptor of the matrix that starts `bytes` further on (a multiple of
+// 16).  The start-address field holds address >> 4 in 14 bits; every shared
+// memory address of a CTA (< 228 KB) stays below its limit, so no carry leaves it.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |

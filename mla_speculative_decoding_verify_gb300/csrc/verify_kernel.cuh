@@ -270,6 +270,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // ================= MMA issuer =================
         const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
         const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+        const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
         bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, 0, abort_flag, lim));
         tc_fence_after();
 
@@ -282,15 +283,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
                 const uint32_t sb = stage0 + st * kStageBytes;
                 const uint32_t pcol = tmem + kTmS + 64 * x;
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc(sb + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-                    mma_ts(tmem + kTmO, pcol + 8 * kk, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                }
+                const uint64_t bv = smem_desc(sb, kChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + kTmO, pcol + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
                 if (lo) {
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t bdesc = smem_desc(sb + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-                        mma_ts(tmem + kTmO, pcol + 32 + 8 * kk, bdesc, idesc_pv, 1u);
-                    }
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts(tmem + kTmO, pcol + 32 + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
                 }
                 mma_commit(&ctl->pv_done[x]);
                 mma_commit(&ctl->kv_empty[st]);
@@ -312,16 +313,16 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (lane == 0) {
                 const uint32_t sb = stage0 + st * kStageBytes;
                 const uint32_t dS = tmem + kTmS + 64 * x;
-                for (int k = 0; k < kDLatentHalf / 16; ++k) {
-                    const uint64_t bdesc =
-                        smem_desc(sb + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024, kSwizzle128B);
-                    mma_ts(dS, tmem + kTmQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
-                }
-                for (int k = 0; k < kDRopeHalf / 16; ++k) {
-                    const uint64_t adesc = smem_desc(qrope_addr + k * 32, 16, 512, kSwizzle64B);
-                    const uint64_t bdesc = smem_desc(sb + 4 * kChunkBytes + k * 32, 16, 512, kSwizzle64B);
-                    mma_ss(dS, adesc, bdesc, idesc_qk, 1u);
-                }
+                // one base descriptor per operand; the k-steps add constant byte offsets
+                const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
+                const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
+#pragma unroll
+                for (int k = 0; k < kDLatentHalf / 16; ++k)
+                    mma_ts(dS, tmem + kTmQ + 8 * k, desc_advance(bk, (k >> 2) * kChunkBytes + (k & 3) * 32),
+                           idesc_qk, k > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < kDRopeHalf / 16; ++k)
+                    mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
                 mma_commit(&ctl->s_full[x]);
             }
             __syncwarp();
@@ -432,18 +433,17 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     s[4 * u + 3] += v.w;
                 }
             }
-            // ---- scale, tree mask ----
+            // ---- tree mask (tiles that reach the draft tokens only) ----
+            // Scores stay unscaled here: the scale is positive, so the row max can be
+            // taken on raw scores and the scale folded into the exponent's FMA below.
             const int kpos = (t0 + jj) * kBlockN;
-            if (kpos + kBlockN <= P) {
-#pragma unroll
-                for (int k = 0; k < kBlockN; ++k) s[k] *= p.scale_log2;
-            } else {
+            if (kpos + kBlockN > P) {
 #pragma unroll
                 for (int k = 0; k < kBlockN; ++k) {
                     const int t = kpos + k;
                     bool vis = t < P;
                     if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
-                    s[k] = vis ? s[k] * p.scale_log2 : -INFINITY;
+                    s[k] = vis ? s[k] : -INFINITY;
                 }
             }
             // tree reductions (8 independent chains) keep the dependent latency short
@@ -452,8 +452,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             for (int k = 0; k < 8; ++k) mx[k] = s[k];
 #pragma unroll
             for (int k = 8; k < kBlockN; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;  // log2 units
             // ---- lazy online-softmax rescale (warp-uniform TMEM traffic) ----
             const bool grow_max = ok && mt > m_use + kLazyRescaleLog2;
             float alpha = 1.f;
@@ -478,20 +479,24 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     }
                 }
             }
-            // ---- probabilities ----
+            // ---- probabilities: p = 2^(s * scale * log2 e - m), one FMA + ex2 each ----
             const bool live = m_use != -INFINITY;
-            float ps[8], pm[8];
+            const float neg_m = -m_use;
+            float ps[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ps[k] = pm[k] = 0.f;
+            for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+            if (live) {
 #pragma unroll
-            for (int k = 0; k < kBlockN; ++k) {
-                s[k] = live ? ex2_approx(s[k] - m_use) : 0.f;
-                ps[k & 7] += s[k];
-                pm[k & 7] = fmaxf(pm[k & 7], s[k]);
+                for (int k = 0; k < kBlockN; ++k) {
+                    s[k] = ex2_approx(fmaf(s[k], p.scale_log2, neg_m));
+                    ps[k & 7] += s[k];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
             }
             const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                     fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            const float pmax = live ? ex2_approx(mt - m_use) : 0.f;  // the tile's largest p
             // One named barrier decides, uniformly for the 128 threads, whether to stop
             // (bit 1) and whether this tile needs the low part of P (bit 0).
             volatile int* flags = &ctl->tile_flags[jj % 3];
@@ -514,26 +519,21 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 ctl->lo_flag[x] = need_lo ? 1 : 0;
             }
             uint32_t hi[32];
-            float ac[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ac[k] = 0.f;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-                ac[k & 7] += bf16lo_to_f32(hi[k]) + bf16hi_to_f32(hi[k]);
-            }
+            for (int k = 0; k < 32; ++k) hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
             tmem_st32(trow + kTmS + 64 * x, hi);
             if (need_lo) {
                 uint32_t lo[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < 32; ++k)
                     lo[k] = pack_bf16x2(s[2 * k] - bf16lo_to_f32(hi[k]), s[2 * k + 1] - bf16hi_to_f32(hi[k]));
-                    ac[k & 7] += bf16lo_to_f32(lo[k]) + bf16hi_to_f32(lo[k]);
-                }
                 tmem_st32(trow + kTmS + 64 * x + 32, lo);
             }
             tmem_wait_st();
-            l += ((ac[0] + ac[1]) + (ac[2] + ac[3])) + ((ac[4] + ac[5]) + (ac[6] + ac[7]));
+            // The normaliser uses the fp32 weights.  Without the low part the bf16
+            // weights that PV sees differ from them by unbiased rounding of at most
+            // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
+            l += psum;
             tc_fence_before();
             mbar_arrive(&ctl->p_full[x]);
         }

@@ -58,6 +58,8 @@ def _call(**over):
     (dict(num_splits=65), binding.MLA_ERR_UNSUPPORTED),
     (dict(batch=-1), binding.MLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.MLA_ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.MLA_ERR_INVALID_ARG),        # a softmax scale is positive
+    (dict(scale=-0.07), binding.MLA_ERR_INVALID_ARG),
     (dict(q_lat=None), binding.MLA_ERR_INVALID_ARG),
     (dict(out=None), binding.MLA_ERR_INVALID_ARG),
     (dict(kv_cache=24), binding.MLA_ERR_INVALID_ARG),   # not 16-byte aligned

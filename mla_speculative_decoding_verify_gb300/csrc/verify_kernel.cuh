@@ -13,10 +13,15 @@
 //     the ancestor bit set of the row's node.
 //   - PV: each CTA accumulates its 256 columns of O = P * c_kv in TMEM (V is
 //     the c_kv latent, so the same shared-memory tile that served as K feeds
-//     PV).  P goes to TMEM as bf16; when a tile carries a large share of a
-//     row's mass a second bf16 "low part" of P is added so the result keeps
-//     close to fp32 weights.
-// TMEM: O [0,256) | q latent half [256,384) | S/P buffers [384,448), [448,512).
+//     PV).  P goes to shared memory as bf16; when a tile carries a large share
+//     of a row's mass a second bf16 "low part" of P is added so the result
+//     keeps close to fp32 weights.
+// Pipeline: the softmax warps read a tile's partial scores out of TMEM as soon
+// as QK has written them and ship them to the peer, then finish the previous
+// tile while the copy is in flight; an S buffer is therefore free again right
+// after it was read, and the QK issuer runs ahead, bounded by the KV ring.  A
+// second MMA warp issues PV as soon as a tile's P is in shared memory.
+// TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
 #pragma once
 
 #include <cuda.h>
@@ -36,7 +41,9 @@ constexpr int kTokensPerTile = kRows / kHeads;
 constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
 constexpr int kStages = 3;
-constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kThreads = 224;          // warp 0 TMA, warp 1 QK MMAs, warps 2..5 softmax, warp 6 PV MMAs
+constexpr int kSoftmaxWarp0 = 2;
+constexpr int kPvWarp = 6;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kChunkBytes = kBlockN * 64 * 2;          // [64 keys][64 dims] bf16, 128B swizzle
 constexpr uint32_t kRopeTileBytes = kBlockN * kDRopeHalf * 2;  // [64 keys][32 dims], 64B swizzle
@@ -45,13 +52,16 @@ constexpr uint32_t kQRopeBytes = kRows * kDRopeHalf * 2;
 constexpr uint32_t kXBufBytes = kRows * kBlockN * 4;       // one partial score tile, fp32
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;          // 2 receive buffers (peer's partials)
-constexpr uint32_t kOffStaging = kOffXBuf + 2 * kXBufBytes;     // own partial, source of the bulk copy
-constexpr uint32_t kOffCtrl = kOffStaging + kXBufBytes;
+constexpr uint32_t kPBytes = kRows * kBlockN * 2;          // one bf16 P tile, K-major, 128B swizzle
+constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;          // receive buffer (the peer's partial)
+constexpr uint32_t kOffStaging = kOffXBuf + kXBufBytes;         // own partial, source of the bulk copy
+constexpr uint32_t kOffP = kOffStaging + kXBufBytes;            // P high part, then P low part
+constexpr uint32_t kOffCtrl = kOffP + 2 * kPBytes;
 constexpr uint32_t kCtrlBytes = 512;
 constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + slack for 1 KB alignment
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B swizzle");
-static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0, "region alignment");
+static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0 && kOffP % 1024 == 0,
+              "region alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
 
 constexpr uint32_t kTmemCols = 512;
@@ -90,14 +100,16 @@ struct Ctrl {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t kv_fixed[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t pv_done[2];
-    uint64_t x_full[2];    // peer's partial for tile j landed in receive buffer j % 2 (bytes)
-    uint64_t x_empty[2];   // peer finished reading the partial this CTA sent into its buffer j % 2
+    uint64_t s_full[2];    // QK wrote S buffer x
+    uint64_t s_free[2];    // the softmax threads read S buffer x (QK may overwrite it)
+    uint64_t p_full[2];    // P of tile j is in shared memory (j & 1 selects the barrier)
+    uint64_t pv_done[2];   // PV of tile j finished (P buffer and O free again)
+    uint64_t x_full;       // the peer's partial of the next tile landed in the receive buffer (bytes)
+    uint64_t x_empty;      // the peer finished reading the partial this CTA sent it
     uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
     uint64_t q_ready;
-    uint64_t drain;
+    uint64_t drain_qk;
+    uint64_t drain_pv;
     uint32_t tmem_base;
     int abort;
     int lo_flag[2];
@@ -148,7 +160,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int r = q4 * 32 + lane;
     const int tok_local = r / kHeads;
     const int head = r % kHeads;
-    const bool row_valid = warp >= 2 && tok_local < ntok;
+    const bool softmax_warp = warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4;
+    const bool row_valid = softmax_warp && tok_local < ntok;
     const int qidx = qbase + tok_local;
     const long long grow = static_cast<long long>(qidx) * kHeads + head;  // global output row
 
@@ -178,19 +191,21 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&ctl->s_full[x], 1);
+            mbar_init(&ctl->s_free[x], kSoftmaxThreads);
             mbar_init(&ctl->p_full[x], kSoftmaxThreads);
             mbar_init(&ctl->pv_done[x], 1);
-            mbar_init(&ctl->x_full[x], 1);
-            mbar_init(&ctl->x_empty[x], 1);
             ctl->lo_flag[x] = 0;
         }
         for (int k = 0; k < 3; ++k) ctl->tile_flags[k] = 0;
+        mbar_init(&ctl->x_full, 1);
+        mbar_init(&ctl->x_empty, 1);
         mbar_init(&ctl->q_ready, kSoftmaxThreads);
-        mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->drain_qk, 1);
+        mbar_init(&ctl->drain_pv, 1);
         mbar_init(&ctl->stg_free, 1);
         ctl->abort = 0;
-        // byte counts of the first two incoming partials, posted before the peer can send
-        for (int x = 0; x < 2 && x < n; ++x) mbar_arrive_expect_tx(&ctl->x_full[x], kXBufBytes);
+        // byte count of the first incoming partial, posted before the peer can send
+        mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
         fence_mbar_init_cluster();
     }
     if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -208,6 +223,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint64_t lim = p.timeout_ns;
     const uint32_t stage0 = smem_u32(smem + kOffStages);
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
+    const uint32_t p_addr = smem_u32(smem + kOffP);
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -267,46 +283,19 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             mbar_wait(&ctl->kv_full[st], (last / kStages) & 1, &zero, lim);
         }
     } else if (warp == 1) {
-        // ================= MMA issuer =================
+        // ================= QK issuer =================
         const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
-        const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
         const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
         bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, 0, abort_flag, lim));
         tc_fence_after();
-
-        auto issue_pv = [&](int i) -> bool {
-            const int x = i & 1;
-            const int st = i % kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (i >> 1) & 1, abort_flag, lim))) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
-                const uint32_t sb = stage0 + st * kStageBytes;
-                const uint32_t pcol = tmem + kTmS + 64 * x;
-                const uint64_t bv = smem_desc(sb, kChunkBytes, 1024, kSwizzle128B);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + kTmO, pcol + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                if (lo) {
-#pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ts(tmem + kTmO, pcol + 32 + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
-                }
-                mma_commit(&ctl->pv_done[x]);
-                mma_commit(&ctl->kv_empty[st]);
-            }
-            __syncwarp();
-            return true;
-        };
-
         for (int jj = 0; jj < n && ok; ++jj) {
             const int st = jj % kStages;
             const int x = jj & 1;
             const bool tail = (t0 + jj) * kBlockN + kBlockN > L;
             ok = tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
                       : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
-            if (ok && jj >= 2) ok = mbar_wait(&ctl->pv_done[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
+            // S buffer x held tile jj - 2; the softmax threads have read it out
+            if (ok && jj >= 2) ok = mbar_wait(&ctl->s_free[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -326,19 +315,54 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 mma_commit(&ctl->s_full[x]);
             }
             __syncwarp();
-            if (jj >= 1) ok = issue_pv(jj - 1);
         }
-        if (ok) ok = issue_pv(n - 1);
         if (!ok) {
             if (lane == 0) raise_status(p.status, kStatusTimeout);
             *abort_flag = 1;
         }
-        // Wait until every MMA issued by this CTA has finished before TMEM is released.
+        // Wait until every MMA issued by this warp has finished before TMEM is released.
         const int zero = 0;
-        if (lane == 0) mma_commit(&ctl->drain);
+        if (lane == 0) mma_commit(&ctl->drain_qk);
         __syncwarp();
-        mbar_wait(&ctl->drain, 0, &zero, lim);
-    } else {
+        mbar_wait(&ctl->drain_qk, 0, &zero, lim);
+    } else if (warp == kPvWarp) {
+        // ================= PV issuer: O[:, half c] += P * V =================
+        const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+        const uint64_t ap_hi = smem_desc(p_addr, 16, 1024, kSwizzle128B);
+        const uint64_t ap_lo = smem_desc(p_addr + kPBytes, 16, 1024, kSwizzle128B);
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+            const int x = i & 1;
+            const int st = i % kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (i >> 1) & 1, abort_flag, lim));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
+                const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                if (lo) {
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                }
+                mma_commit(&ctl->pv_done[x]);
+                mma_commit(&ctl->kv_empty[st]);
+            }
+            __syncwarp();
+        }
+        if (!ok) {
+            if (lane == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
+        }
+        const int zero = 0;
+        if (lane == 0) mma_commit(&ctl->drain_pv);
+        __syncwarp();
+        mbar_wait(&ctl->drain_pv, 0, &zero, lim);
+    } else if (softmax_warp) {
         // ================= softmax / epilogue (thread = row) =================
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
@@ -368,74 +392,94 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             mbar_arrive(&ctl->q_ready);
         }
 
-        const int node = kTokensPerTile * tile + tok_local;
         const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
         const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
         const uint32_t xbuf_peer = mapa(xbuf_local, peer);
         const uint32_t stg_local = smem_u32(smem + kOffStaging);
-        const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full[0]), peer);
-        int posted = n < 2 ? n : 2;  // incoming partials whose byte count is posted (thread r == 0)
-        int consumed = 0;            // incoming partials waited for (thread r == 0)
+        const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full), peer);
+        const uint32_t rowbase = stg_local + r * (kBlockN * 4);       // this row in the staging buffer
+        const uint32_t peerbase = xbuf_local + r * (kBlockN * 4);     // this row in the receive buffer
+        const uint32_t prow = p_addr + r * 128;                       // this row of P (128 bytes)
+        int posted = 1;    // incoming partials whose byte count is posted (thread r == 0)
+        int consumed = 0;  // incoming partials waited for (thread r == 0)
         float m_use = -INFINITY;
         float l = 0.f;
         bool ok = true;
-        (void)node;
 
-        for (int jj = 0; jj < n; ++jj) {
-            const int x = jj & 1;
-            const uint32_t ph = (jj >> 1) & 1;
-            // Wait outcomes are made warp-uniform (tcgen05.ld/st are warp-collective);
-            // the per-tile flag word below makes the stop decision uniform over all
-            // 128 softmax threads before they touch the next named barrier.
-            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], ph, abort_flag, lim));
-            float s[kBlockN];
+        // Step C of tile t: partial scores TMEM -> staging -> the peer's receive buffer.
+        // Every softmax thread takes part in the named barrier, whatever its `ok`.
+        auto stage_and_send = [&](int t) {
+            const int x = t & 1;
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&ctl->s_full[x], (t >> 1) & 1, abort_flag, lim));
+            // the peer has received the previous partial: the staging buffer may be overwritten
+            if (ok && t >= 1) ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->stg_free, (t - 1) & 1, abort_flag, lim));
             if (ok) {
                 tc_fence_after();
-                uint32_t a[32], bb[32];
-                tmem_ld32(trow + kTmS + 64 * x, a);
-                tmem_ld32(trow + kTmS + 64 * x + 32, bb);
-                tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    s[k] = __uint_as_float(a[k]);
-                    s[32 + k] = __uint_as_float(bb[k]);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t a[32];
+                    tmem_ld32(trow + kTmS + 64 * x + 32 * half, a);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int uu = 8 * half + u;
+                        st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
+                                     __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
+                                     __uint_as_float(a[4 * u + 3]));
+                    }
                 }
-            }
-            // ---- exchange partial scores with the peer CTA ----
-            // own partial -> staging (local) -> TMA bulk copy into the peer's receive
-            // buffer, bytes counted on the peer's x_full; then read the peer's partial.
-            if (ok && jj >= 1) ok = mbar_wait<true>(&ctl->stg_free, (jj - 1) & 1, abort_flag, lim);
-            if (ok) {
-                const uint32_t rowbase = stg_local + r * (kBlockN * 4);
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    st_shared_v4(rowbase + ((u ^ (r & 7)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+                tc_fence_before();
+                mbar_arrive(&ctl->s_free[x]);  // S buffer x may take the next QK
                 fence_proxy_async_smem();
             }
             named_bar_sync(3, kSoftmaxThreads);
             if (r == 0 && ok) {
-                if (jj >= 2) ok = mbar_wait<true>(&ctl->x_empty[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
-                if (ok) bulk_copy_to_peer(xbuf_peer + x * kXBufBytes, stg_local, kXBufBytes, xfull_peer + 8u * x);
+                // the peer has read the partial this CTA sent before (its receive buffer is free)
+                if (t >= 1) ok = mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
+                if (ok) bulk_copy_to_peer(xbuf_peer, stg_local, kXBufBytes, xfull_peer);
             }
-            if (ok) ok = mbar_wait<true>(&ctl->x_full[x], ph, abort_flag, lim);
+        };
+
+        if (n > 0) stage_and_send(0);
+        for (int jj = 0; jj < n; ++jj) {
+            const int x = jj & 1;
+            // ---- A/B: full scores = own partial (staging) + the peer's (receive buffer) ----
+            if (ok) ok = mbar_wait<true>(&ctl->x_full, jj & 1, abort_flag, lim);
+            float s[kBlockN];
             if (ok) {
                 if (r == 0) {
                     ++consumed;
                     mbar_arrive_remote_relaxed(&ctl->stg_free, peer);  // our staging landed: peer may reuse its own
                 }
-                const uint32_t rowbase = xbuf_local + x * kXBufBytes + r * (kBlockN * 4);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const float4 v = ld_shared_v4(rowbase + ((u ^ (r & 7)) << 4));
-                    s[4 * u] += v.x;
-                    s[4 * u + 1] += v.y;
-                    s[4 * u + 2] += v.z;
-                    s[4 * u + 3] += v.w;
+                    const uint32_t sw = (u ^ (r & 7)) << 4;
+                    const float4 a = ld_shared_v4(rowbase + sw);
+                    const float4 v = ld_shared_v4(peerbase + sw);
+                    s[4 * u] = a.x + v.x;
+                    s[4 * u + 1] = a.y + v.y;
+                    s[4 * u + 2] = a.z + v.z;
+                    s[4 * u + 3] = a.w + v.w;
                 }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
             }
-            // ---- tree mask (tiles that reach the draft tokens only) ----
-            // Scores stay unscaled here: the scale is positive, so the row max can be
-            // taken on raw scores and the scale folded into the exponent's FMA below.
+            // the receive buffer has been read by all 128 threads: let the peer send the next tile
+            named_bar_sync(2, kSoftmaxThreads);
+            if (r == 0 && ok) {
+                if (jj + 1 < n) {
+                    mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
+                    ++posted;
+                }
+                mbar_arrive_remote_relaxed(&ctl->x_empty, peer);
+            }
+            // ---- C: ship the next tile's partial scores; its copy overlaps this tile's math ----
+            if (jj + 1 < n) stage_and_send(jj + 1);
+            // ---- D: this tile's softmax ----
+            // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
+            // the scale is positive, so the row max can be taken on raw scores and the scale
+            // folded into the exponent's FMA below.
             const int kpos = (t0 + jj) * kBlockN;
             if (kpos + kBlockN > P) {
 #pragma unroll
@@ -464,20 +508,22 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 l *= alpha;
             }
             ok = __all_sync(0xffffffffu, ok);
-            if (ok && jj > 0 && __any_sync(0xffffffffu, grow_max)) {
+            // PV of the previous tile must be done before O is rescaled and before its
+            // P buffer is overwritten (it normally finished long ago)
+            if (ok && jj > 0)
                 ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1,
                                                        abort_flag, lim));
-                if (ok) {
-                    tc_fence_after();
-                    for (int part = 0; part < kDLatentHalf / 32; ++part) {
-                        uint32_t o[32];
-                        tmem_ld32(trow + kTmO + 32 * part, o);
-                        tmem_wait_ld();
+            if (ok && jj > 0 && __any_sync(0xffffffffu, grow_max)) {
+                tc_fence_after();
+                for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                    uint32_t o[32];
+                    tmem_ld32(trow + kTmO + 32 * part, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st32(trow + kTmO + 32 * part, o);
-                    }
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(trow + kTmO + 32 * part, o);
                 }
+                tmem_wait_st();
             }
             // ---- probabilities: p = 2^(s * scale * log2 e - m), one FMA + ex2 each ----
             const bool live = m_use != -INFINITY;
@@ -511,30 +557,37 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             const bool need_lo = tf & 1;
             if (r == 0) {
                 ctl->tile_flags[(jj + 2) % 3] = 0;  // read by everyone before this barrier; next used by tile jj + 2
-                if (jj + 2 < n) {
-                    mbar_arrive_expect_tx(&ctl->x_full[x], kXBufBytes);  // re-arm for tile jj + 2
-                    ++posted;
-                }
-                mbar_arrive_remote_relaxed(&ctl->x_empty[x], peer);  // receive buffer x read by all
                 ctl->lo_flag[x] = need_lo ? 1 : 0;
             }
-            uint32_t hi[32];
+            // ---- P -> shared memory (K-major rows of 64 keys, 128-byte swizzle) ----
 #pragma unroll
-            for (int k = 0; k < 32; ++k) hi[k] = pack_bf16x2(s[2 * k], s[2 * k + 1]);
-            tmem_st32(trow + kTmS + 64 * x, hi);
-            if (need_lo) {
-                uint32_t lo[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    lo[k] = pack_bf16x2(s[2 * k] - bf16lo_to_f32(hi[k]), s[2 * k + 1] - bf16hi_to_f32(hi[k]));
-                tmem_st32(trow + kTmS + 64 * x + 32, lo);
+            for (int u = 0; u < 8; ++u) {
+                uint4 w;
+                w.x = pack_bf16x2(s[8 * u + 0], s[8 * u + 1]);
+                w.y = pack_bf16x2(s[8 * u + 2], s[8 * u + 3]);
+                w.z = pack_bf16x2(s[8 * u + 4], s[8 * u + 5]);
+                w.w = pack_bf16x2(s[8 * u + 6], s[8 * u + 7]);
+                const uint32_t off = (u ^ (r & 7)) << 4;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off), "r"(w.x), "r"(w.y),
+                             "r"(w.z), "r"(w.w)
+                             : "memory");
+                if (need_lo) {
+                    uint4 v;
+                    v.x = pack_bf16x2(s[8 * u + 0] - bf16lo_to_f32(w.x), s[8 * u + 1] - bf16hi_to_f32(w.x));
+                    v.y = pack_bf16x2(s[8 * u + 2] - bf16lo_to_f32(w.y), s[8 * u + 3] - bf16hi_to_f32(w.y));
+                    v.z = pack_bf16x2(s[8 * u + 4] - bf16lo_to_f32(w.z), s[8 * u + 5] - bf16hi_to_f32(w.z));
+                    v.w = pack_bf16x2(s[8 * u + 6] - bf16lo_to_f32(w.w), s[8 * u + 7] - bf16hi_to_f32(w.w));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + kPBytes + off), "r"(v.x),
+                                 "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
             }
-            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
             // The normaliser uses the fp32 weights.  Without the low part the bf16
             // weights that PV sees differ from them by unbiased rounding of at most
             // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
             l += psum;
-            tc_fence_before();
             mbar_arrive(&ctl->p_full[x]);
         }
 
@@ -546,7 +599,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 raise_status(p.status, kStatusTimeout);
                 // do not leave while the peer's bulk copies may still land in this CTA
                 const int zero = 0;
-                for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full[t & 1], (t >> 1) & 1, &zero, lim);
+                for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
         } else {

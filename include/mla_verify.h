@@ -181,6 +181,53 @@ int mla_verify_attn_noalloc(const void *q_lat, const void *q_rope, const void *k
                             int page_size, int num_pages, int max_pages_per_seq);
 
 /*
+ * Paged-cache steps around verification ("The Shared Memory Ceiling", section
+ * "The Broader Context": the draft tree's latents live in the same paged KV
+ * cache that verification reads, and the step after it is a KV-cache defrag).
+ * Rows are 576 bf16 values (c_kv then k_rope) moved as raw bits: exact.
+ * Request b's tree region is KV positions P_b .. P_b + n_tree[b] - 1 with
+ * P_b = seq_lens[b] - n_tree[b], mapped through block_table as for
+ * mla_verify_attn; it must lie in pages no other request writes.
+ *
+ * mla_tree_kv_workspace_size: bytes of workspace both steps need (the device
+ * status word, readable with mla_read_status).
+ *
+ * mla_tree_kv_append: writes tree_kv (device bf16 [total_q, 576], tokens back
+ * to back in request order, as in q_lat) into each request's tree region of
+ * kv_cache ([num_pages, page_size, 576], 16-byte aligned).  A request whose
+ * n_tree is outside [0, 64] or above its seq_len sets status bit
+ * 1 << MLA_ERR_BAD_TREE; one whose tree region maps to a block id outside
+ * [0, num_pages) sets 1 << MLA_ERR_BAD_BLOCK; either request is left untouched.
+ *
+ * mla_tree_kv_accept: after verification, accept_len[b] (device int32 [batch])
+ * tokens of request b are accepted; accept_idx (device int32 [total_q], same
+ * layout as tree_parent) holds, at the start of each request's segment, their
+ * node indices along a path from a root (the first one's parent is -1, each
+ * next one is a child of the one before).  Accepted node k's row moves to
+ * position P_b + k; rows after P_b + accept_len[b] keep their old contents,
+ * and new_seq_lens[b] (device int32 [batch]) = P_b + accept_len[b].  All of a
+ * request's accepted rows are read before any is written.  A malformed tree or
+ * path, or accept_len outside [0, n_tree[b]], sets 1 << MLA_ERR_BAD_TREE; a bad
+ * block id sets 1 << MLA_ERR_BAD_BLOCK; such a request is left untouched and
+ * new_seq_lens[b] = seq_lens[b].
+ *
+ * Both: one thread block per request on `stream`; mla_init must have run on
+ * the device; host-checkable errors return before any launch; the workspace
+ * (caller-owned, >= mla_tree_kv_workspace_size() bytes) is cleared on the
+ * stream first.  They allocate nothing and never synchronise.
+ */
+size_t mla_tree_kv_workspace_size(void);
+int mla_tree_kv_append(const void *tree_kv, void *kv_cache, const int32_t *block_table,
+                       const int32_t *seq_lens, const int32_t *n_tree, cudaStream_t stream,
+                       int batch, int total_q, int page_size, int num_pages, int max_pages_per_seq,
+                       void *workspace, size_t workspace_bytes);
+int mla_tree_kv_accept(void *kv_cache, const int32_t *block_table, const int32_t *seq_lens,
+                       const int32_t *n_tree, const int32_t *tree_parent, const int32_t *accept_len,
+                       const int32_t *accept_idx, int32_t *new_seq_lens, cudaStream_t stream,
+                       int batch, int total_q, int page_size, int num_pages, int max_pages_per_seq,
+                       void *workspace, size_t workspace_bytes);
+
+/*
  * Measurement hook: while set, every mla_verify_attn call records `begin`
  * immediately before and `end` immediately after the launch of its fused
  * verify kernel, on the call's stream, so the kernel can be timed alone.

@@ -33,7 +33,8 @@ MAX_SPLITS = 64
 
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
-            "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc")
+            "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc",
+            "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -78,6 +79,12 @@ def lib() -> ctypes.CDLL:
         L.mla_set_profile_events.argtypes = [vp, vp]
         L.mla_read_status.restype = i32
         L.mla_read_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.mla_tree_kv_workspace_size.restype = sz
+        L.mla_tree_kv_workspace_size.argtypes = []
+        L.mla_tree_kv_append.restype = i32
+        L.mla_tree_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz]
+        L.mla_tree_kv_accept.restype = i32
+        L.mla_tree_kv_accept.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz]
         _lib = L
         return L
 
@@ -141,6 +148,27 @@ def set_profile_events(begin, end) -> None:
     check(lib().mla_set_profile_events(begin, end), "mla_set_profile_events")
 
 
+def tree_kv_workspace_size() -> int:
+    return int(lib().mla_tree_kv_workspace_size())
+
+
+def tree_kv_append(tree_kv, kv_cache, block_table, seq_lens, n_tree, stream, batch, total_q, page_size,
+                   num_pages, max_pages_per_seq, workspace, workspace_bytes) -> int:
+    """Raw call: write the draft tree's latents into the paged cache; returns the status."""
+    return int(lib().mla_tree_kv_append(tree_kv, kv_cache, block_table, seq_lens, n_tree, stream, batch,
+                                        total_q, page_size, num_pages, max_pages_per_seq, workspace,
+                                        workspace_bytes))
+
+
+def tree_kv_accept(kv_cache, block_table, seq_lens, n_tree, tree_parent, accept_len, accept_idx,
+                   new_seq_lens, stream, batch, total_q, page_size, num_pages, max_pages_per_seq,
+                   workspace, workspace_bytes) -> int:
+    """Raw call: compact the accepted path of each request's tree; returns the status."""
+    return int(lib().mla_tree_kv_accept(kv_cache, block_table, seq_lens, n_tree, tree_parent, accept_len,
+                                        accept_idx, new_seq_lens, stream, batch, total_q, page_size,
+                                        num_pages, max_pages_per_seq, workspace, workspace_bytes))
+
+
 def read_status(workspace) -> int:
     v = ctypes.c_int(0)
     check(lib().mla_read_status(workspace, ctypes.byref(v)), "mla_read_status")
@@ -195,3 +223,37 @@ def verify(db: "DeviceBatch", num_splits_req: int = 0, out=None, lse=None, works
                        workspace.data_ptr(), workspace.numel())
     check(code, "mla_verify_attn")
     return out, lse, workspace
+
+
+def append_tree(db: "DeviceBatch", tree_kv, workspace=None, stream=None):
+    """Write tree_kv (torch int16 [total_q, 576] on the device) into db.kv_cache; returns the workspace."""
+    import torch
+    inp = db.inp
+    if workspace is None:
+        workspace = torch.empty(tree_kv_workspace_size(), dtype=torch.uint8, device=db.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(db.device)
+    check(tree_kv_append(tree_kv.data_ptr(), db.kv_cache.data_ptr(), db.block_table.data_ptr(),
+                         db.seq_lens.data_ptr(), db.n_tree.data_ptr(), stream.cuda_stream, inp.batch,
+                         inp.total_q, inp.page_size, inp.num_pages, inp.max_pages_per_seq,
+                         workspace.data_ptr(), workspace.numel()), "mla_tree_kv_append")
+    return workspace
+
+
+def accept_path(db: "DeviceBatch", accept_len, accept_idx, new_seq_lens=None, workspace=None, stream=None):
+    """Compact the accepted paths (torch int32 device tensors) in db.kv_cache; returns
+    (new_seq_lens, workspace)."""
+    import torch
+    inp = db.inp
+    if new_seq_lens is None:
+        new_seq_lens = torch.empty(inp.batch, dtype=torch.int32, device=db.device)
+    if workspace is None:
+        workspace = torch.empty(tree_kv_workspace_size(), dtype=torch.uint8, device=db.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(db.device)
+    check(tree_kv_accept(db.kv_cache.data_ptr(), db.block_table.data_ptr(), db.seq_lens.data_ptr(),
+                         db.n_tree.data_ptr(), db.tree_parent.data_ptr(), accept_len.data_ptr(),
+                         accept_idx.data_ptr(), new_seq_lens.data_ptr(), stream.cuda_stream, inp.batch,
+                         inp.total_q, inp.page_size, inp.num_pages, inp.max_pages_per_seq,
+                         workspace.data_ptr(), workspace.numel()), "mla_tree_kv_accept")
+    return new_seq_lens, workspace

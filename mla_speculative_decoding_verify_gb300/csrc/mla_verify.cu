@@ -12,6 +12,7 @@
 
 #include "mla_verify.h"
 #include "combine_kernel.cuh"
+#include "kv_ops_kernel.cuh"
 #include "prep_kernel.cuh"
 #include "verify_kernel.cuh"
 
@@ -179,6 +180,9 @@ int mla_init(int device) {
             return MLA_ERR_CUDA;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    if (cudaFuncSetAttribute(mla::mla_tree_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mla::kAcceptSmemBytes)) != cudaSuccess)
+        return MLA_ERR_CUDA;
     if (cudaFuncSetAttribute(mla::mla_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
         return MLA_ERR_CUDA;
@@ -318,6 +322,70 @@ int mla_set_profile_events(cudaEvent_t begin, cudaEvent_t end) {
     g_prof_begin = begin;
     g_prof_end = end;
     return MLA_OK;
+}
+
+// Shared argument checks of the two paged-cache steps; fills the common parameters.
+static int kv_op_setup(void* kv_cache, const int32_t* block_table, const int32_t* seq_lens, const int32_t* n_tree,
+                       int batch, int total_q, int page_size, int num_pages, int max_pages_per_seq, void* workspace,
+                       size_t workspace_bytes, mla::KvOpParams* kp) {
+    if (batch < 0 || total_q < 0 || page_size <= 0 || num_pages < 0 || max_pages_per_seq < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < sizeof(int) || (reinterpret_cast<uintptr_t>(workspace) & 3u))
+        return MLA_ERR_WORKSPACE;
+    if (batch > 0 && (!kv_cache || !block_table || !seq_lens || !n_tree || num_pages == 0 || max_pages_per_seq == 0))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(kv_cache)) return MLA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MLA_ERR_NOT_INITIALIZED;
+    *kp = mla::KvOpParams{};
+    kp->cache = static_cast<uint4*>(kv_cache);
+    kp->block_table = block_table;
+    kp->seq_lens = seq_lens;
+    kp->n_tree = n_tree;
+    kp->status = static_cast<int*>(workspace);
+    kp->batch = batch;
+    kp->page_size = page_size;
+    kp->max_pages = max_pages_per_seq;
+    kp->num_pages = num_pages;
+    return MLA_OK;
+}
+
+size_t mla_tree_kv_workspace_size(void) { return 256; }
+
+int mla_tree_kv_append(const void* tree_kv, void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                       const int32_t* n_tree, cudaStream_t stream, int batch, int total_q, int page_size,
+                       int num_pages, int max_pages_per_seq, void* workspace, size_t workspace_bytes) {
+    mla::KvOpParams kp;
+    const int rc = kv_op_setup(kv_cache, block_table, seq_lens, n_tree, batch, total_q, page_size, num_pages,
+                               max_pages_per_seq, workspace, workspace_bytes, &kp);
+    if (rc != MLA_OK) return rc;
+    if (batch > 0 && total_q > 0 && (!tree_kv || !aligned16(tree_kv))) return MLA_ERR_INVALID_ARG;
+    kp.tree_kv = static_cast<const uint4*>(tree_kv);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (batch == 0) return MLA_OK;
+    mla::mla_tree_append_kernel<<<batch, mla::kKvOpThreads, 0, stream>>>(kp);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_tree_kv_accept(void* kv_cache, const int32_t* block_table, const int32_t* seq_lens, const int32_t* n_tree,
+                       const int32_t* tree_parent, const int32_t* accept_len, const int32_t* accept_idx,
+                       int32_t* new_seq_lens, cudaStream_t stream, int batch, int total_q, int page_size,
+                       int num_pages, int max_pages_per_seq, void* workspace, size_t workspace_bytes) {
+    mla::KvOpParams kp;
+    const int rc = kv_op_setup(kv_cache, block_table, seq_lens, n_tree, batch, total_q, page_size, num_pages,
+                               max_pages_per_seq, workspace, workspace_bytes, &kp);
+    if (rc != MLA_OK) return rc;
+    if (batch > 0 && (!accept_len || !new_seq_lens || (total_q > 0 && (!tree_parent || !accept_idx))))
+        return MLA_ERR_INVALID_ARG;
+    kp.tree_parent = tree_parent;
+    kp.accept_len = accept_len;
+    kp.accept_idx = accept_idx;
+    kp.new_seq_lens = new_seq_lens;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (batch == 0) return MLA_OK;
+    mla::mla_tree_accept_kernel<<<batch, mla::kKvOpThreads, mla::kAcceptSmemBytes, stream>>>(kp);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int mla_read_status(const void* workspace, int* device_status) {

@@ -86,3 +86,39 @@ def test_split_heuristic_and_workspace(lib):
     w4 = binding.workspace_size(16, 512, 32, 16416, splits=4)
     assert w4 - w1 >= 4 * 512 * 64 * 512 * 4
     assert binding.workspace_size(1, 1, 1, 1, num_heads=32) == 0
+
+
+def _kv_call(op, **over):
+    args = dict(tree_kv=16, kv_cache=16, block_table=16, seq_lens=16, n_tree=16, tree_parent=16, accept_len=16,
+                accept_idx=16, new_seq_lens=16, stream=None, batch=1, total_q=1, page_size=64, num_pages=2,
+                max_pages_per_seq=2, workspace=256, workspace_bytes=256)
+    args.update(over)
+    if op == "append":
+        return binding.tree_kv_append(args["tree_kv"], args["kv_cache"], args["block_table"], args["seq_lens"],
+                                      args["n_tree"], args["stream"], args["batch"], args["total_q"],
+                                      args["page_size"], args["num_pages"], args["max_pages_per_seq"],
+                                      args["workspace"], args["workspace_bytes"])
+    return binding.tree_kv_accept(args["kv_cache"], args["block_table"], args["seq_lens"], args["n_tree"],
+                                  args["tree_parent"], args["accept_len"], args["accept_idx"], args["new_seq_lens"],
+                                  args["stream"], args["batch"], args["total_q"], args["page_size"],
+                                  args["num_pages"], args["max_pages_per_seq"], args["workspace"],
+                                  args["workspace_bytes"])
+
+
+@pytest.mark.parametrize("op", ["append", "accept"])
+@pytest.mark.parametrize("over,code", [
+    (dict(batch=-1), binding.MLA_ERR_INVALID_ARG),
+    (dict(page_size=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(workspace=None), binding.MLA_ERR_WORKSPACE),
+    (dict(workspace_bytes=2), binding.MLA_ERR_WORKSPACE),
+    (dict(kv_cache=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(kv_cache=24), binding.MLA_ERR_INVALID_ARG),     # not 16-byte aligned
+    (dict(num_pages=0), binding.MLA_ERR_INVALID_ARG),
+])
+def test_kv_op_host_argument_checks(lib, op, over, code):
+    assert _kv_call(op, **over) == code
+
+
+def test_kv_op_specific_pointer_checks(lib):
+    assert _kv_call("append", tree_kv=None) in (binding.MLA_ERR_INVALID_ARG, binding.MLA_ERR_NOT_INITIALIZED)
+    assert binding.tree_kv_workspace_size() >= 4

@@ -9,6 +9,7 @@ roofline target applies.  ``--workload`` selects another one.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3] [--splits S]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
+  python bench.py --path append|accept   # the paged-cache steps around verify (GB/s)
 
 For N > 1 (torchrun) every rank runs an independent replica of the workload
 on its own GPU (the path has no exchange step); value = all ranks' work over
@@ -41,12 +42,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["verify", "append", "accept"], default="verify",
+                    help="verify attention (default) or a paged-cache step around it")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
     ap.add_argument("--splits", type=int, default=None, help="KV splits (0 = library's choice)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="oracle rows timed for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=12288, help="oracle rows timed for cpu_baseline (about 10 s)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -345,6 +348,126 @@ def run_ours(args, ranks: Ranks):
     return result
 
 
+# ------------------------------------------------------------------ paged-cache steps
+
+def run_kv_op(args, ranks: Ranks):
+    """Time mla_tree_kv_append or mla_tree_kv_accept on the workload's cache.
+    Algorithmic bytes: every moved 1152-byte row is read once and written once."""
+    import numpy as np
+    import torch
+
+    from mla_speculative_decoding_verify_gb300 import binding, inputs as I
+    from oracle import kv_ops
+
+    op = args.path
+    dev = torch.device(f"cuda:{ranks.local}")
+    torch.cuda.set_device(dev)
+    binding.init(ranks.local)
+    inp = I.config_inputs(WORKLOADS[args.workload], seed=args.seed)
+    db = binding.DeviceBatch(inp, dev)
+    rows = I.tree_rows(inp, seed=args.seed + 1)
+    acc_len, acc_idx = I.accept_paths(inp, seed=args.seed + 2)
+    moved = inp.total_q if op == "append" else int(acc_len.sum())
+    algo_bytes = 2 * moved * 1152
+    d_rows = torch.from_numpy(rows.view(np.int16)).to(dev)
+    d_len = torch.from_numpy(acc_len).to(dev)
+    d_idx = torch.from_numpy(acc_idx).to(dev)
+    new_lens = torch.empty(inp.batch, dtype=torch.int32, device=dev)
+    ws = torch.empty(binding.tree_kv_workspace_size(), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if op == "append":
+            binding.append_tree(db, d_rows, workspace=ws, stream=stream)
+        else:
+            binding.accept_path(db, d_len, d_idx, new_seq_lens=new_lens, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    status = binding.read_status(ws.data_ptr())
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(ranks.local)
+    clocks.start()
+    time.sleep(0.3)
+    ranks.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ranks.barrier()
+    clk = clocks.stop()
+    t = ranks.max(sum(a.elapsed_time(b) for a, b in ev) / K, dev)
+
+    # end to end: the step's inputs from pinned host memory, its result back
+    h_rows = torch.from_numpy(rows.view(np.int16)).pin_memory()
+    h_len = torch.from_numpy(acc_len).pin_memory()
+    h_idx = torch.from_numpy(acc_idx).pin_memory()
+    h_out = torch.empty(inp.batch, dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        if op == "append":
+            d_rows.copy_(h_rows, non_blocking=True)
+        else:
+            d_len.copy_(h_len, non_blocking=True)
+            d_idx.copy_(h_idx, non_blocking=True)
+        step()
+        h_out.copy_(new_lens if op == "accept" else db.seq_lens, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        e2e_step()
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = ranks.max(sum(a.elapsed_time(b) for a, b in ev2) / K, dev)
+    h2d = rows.nbytes if op == "append" else acc_len.nbytes + acc_idx.nbytes
+
+    peaks, peak_kind = measured_peaks()
+    gbs = ranks.world * algo_bytes / (t * 1e-3) / 1e9
+    result = {
+        "metric": f"tree-KV {op} GB/s (paged cache, rows moved read+write), 1 GB300",
+        "value": gbs, "unit": "GB/s", "n_gpus": ranks.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic",
+        "config": {"workload": inp.name, "op": op, "batch": inp.batch, "tree_tokens": inp.total_q,
+                   "rows_moved": moved, "page_size": inp.page_size, "seed": args.seed,
+                   "parallelism": f"replicas x{ranks.world}",
+                   "l2": "flushed between timed steps (256 MiB write, not timed)"},
+        "roofline": {"bound": "hbm", "achieved": gbs / ranks.world, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": gbs / ranks.world / float(peaks["hbm_gbs"]), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs, MEASURED_PEAKS.json" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "kernel": f"mla_tree_{op}_kernel", "bytes_per_launch": algo_bytes},
+        "e2e": {"value": ranks.world * algo_bytes / (t_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(h_out.numel() * 4), "ms_per_step": t_e2e},
+        "gpu_launches": K,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if ranks.rank == 0 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        if op == "append":
+            kv_ops.tree_kv_append(inp.kv_cache, inp.block_table, inp.seq_lens, inp.n_tree, rows, inp.page_size)
+        else:
+            kv_ops.tree_kv_accept(inp.kv_cache, inp.block_table, inp.seq_lens, inp.n_tree, inp.tree_parent,
+                                  acc_len, acc_idx, inp.page_size)
+        dt = time.perf_counter() - t0
+        result["cpu_baseline"] = {"value": algo_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"the whole step (numpy oracle, copies the {inp.kv_cache.nbytes >> 20} MiB "
+                                            f"cache first), {dt:.3f} s"}
+    return result
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, ranks: Ranks):
@@ -395,7 +518,7 @@ def main(argv=None):
         return 0
     ranks = Ranks("nccl")
     try:
-        res = run_ours(args, ranks)
+        res = run_ours(args, ranks) if args.path == "verify" else run_kv_op(args, ranks)
         if ranks.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

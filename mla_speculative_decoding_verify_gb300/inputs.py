@@ -340,3 +340,33 @@ def sample_rows(inp: VerifyInputs, n: int, seed: int = 1234) -> np.ndarray:
     pick = rng.choice(total, size=min(n, total), replace=False) if total else np.zeros(0)
     return np.unique(np.concatenate([np.asarray(must, dtype=np.int64),
                                      np.asarray(pick, dtype=np.int64)]))
+
+
+def tree_rows(inp: VerifyInputs, seed: int = 0) -> np.ndarray:
+    """Seeded latent rows for the draft tree tokens: bf16 bits [total_q, 576] drawn
+    like the cache (N(0,1) rounded to bf16)."""
+    rng = np.random.default_rng(seed)
+    return bf16_bits_from_f32(rng.standard_normal((inp.total_q, 576), dtype=np.float32))
+
+
+def accept_paths(inp: VerifyInputs, seed: int = 0):
+    """Seeded accepted paths: per request a random node, its root-to-node path,
+    cut at a random length (possibly 0).  Returns (accept_len int32 [batch],
+    accept_idx int32 [total_q]) in the layout of tree_parent."""
+    rng = np.random.default_rng(seed)
+    off = inp.q_offsets
+    acc_len = np.zeros(inp.batch, dtype=np.int32)
+    acc_idx = np.full(inp.total_q, -1, dtype=np.int32)
+    for b in range(inp.batch):
+        T = int(inp.n_tree[b])
+        if T == 0:
+            continue
+        par = inp.tree_parent[off[b]:off[b] + T]
+        node, path = int(rng.integers(0, T)), []
+        while node >= 0:
+            path.append(node)
+            node = int(par[node])
+        path = path[::-1][: int(rng.integers(0, len(path) + 1))]
+        acc_len[b] = len(path)
+        acc_idx[off[b]:off[b] + len(path)] = path
+    return acc_len, acc_idx

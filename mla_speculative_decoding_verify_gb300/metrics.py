@@ -53,13 +53,16 @@ def io_bytes(inp) -> dict:
     return {"h2d": int(inputs), "d2h": int(outputs)}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; profile figures taken on other sources are stale."""
+VERIFY_KERNEL_SOURCES = ("sm103_ptx.cuh", "verify_kernel.cuh")
+
+
+def kernel_source_hash(files=VERIFY_KERNEL_SOURCES) -> str:
+    """Hash of the sources the fused verify kernel is compiled from; profile
+    figures taken on other sources are stale."""
     here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(here)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(here, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in sorted(files):
+        with open(os.path.join(here, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]

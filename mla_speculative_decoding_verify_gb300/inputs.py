@@ -370,3 +370,31 @@ def accept_paths(inp: VerifyInputs, seed: int = 0):
         acc_len[b] = len(path)
         acc_idx[off[b]:off[b] + len(path)] = path
     return acc_len, acc_idx
+
+
+def topk_indices(inp: VerifyInputs, topk: int, seed: int = 0, unused_frac: float = 0.0,
+                 duplicates: bool = False) -> np.ndarray:
+    """Seeded top-k slot lists, int32 [total_q, topk]: per tree token, distinct
+    prefix positions in random order (all of them, then -1, when the prefix is
+    shorter than topk).  `unused_frac` of the slots become -1; `duplicates`
+    repeats some listed positions in other slots."""
+    rng = np.random.default_rng(seed)
+    out = np.full((inp.total_q, topk), -1, dtype=np.int32)
+    off = inp.q_offsets
+    for b in range(inp.batch):
+        P = int(inp.seq_lens[b] - inp.n_tree[b])
+        for g in range(int(off[b]), int(off[b + 1])):
+            if P <= 0:
+                continue
+            k = min(topk, P)
+            pos = rng.choice(P, size=k, replace=False) if P > 4 * k else rng.permutation(P)[:k]
+            row = np.full(topk, -1, dtype=np.int64)
+            row[:k] = pos
+            if duplicates and k > 1:
+                n_dup = max(1, k // 8)
+                row[rng.choice(topk, size=n_dup, replace=False)] = rng.choice(pos, size=n_dup)
+            if unused_frac > 0:
+                row[rng.random(topk) < unused_frac] = -1
+            out[g] = rng.permutation(row)
+    return out
+

@@ -25,7 +25,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LOCK = threading.Lock()
 _LIBS = {}
 
-STATUS = {0: "ok", 1: "invalid argument", 6: "bad tree", 7: "bad block id"}
+STATUS = {0: "ok", 1: "invalid argument", 6: "bad tree", 7: "bad block id", 9: "bad top-k index"}
 INT64_MAX = (1 << 63) - 1
 
 
@@ -62,6 +62,10 @@ def load(mutant: int = 0) -> ctypes.CDLL:
                                                ctypes.c_double, i64, i64, i64, i64, i64, i64,
                                                i64, i64, i64p, i64, i64, i64, f64p, f64p,
                                                ctypes.c_int]
+        lib.mla_oracle_verify_sparse_rows.restype = ctypes.c_int
+        lib.mla_oracle_verify_sparse_rows.argtypes = [u16p, u16p, u16p, i32p, i32p, i32p, i32p, i32p, i64,
+                                                      ctypes.c_double, i64, i64, i64, i64, i64, i64, i64,
+                                                      i64, i64p, i64, f64p, f64p, ctypes.c_int]
         lib.mla_oracle_combine.restype = ctypes.c_int
         lib.mla_oracle_combine.argtypes = [f64p, f64p, i64, i64, i64, f64p, f64p]
         lib.mla_oracle_check.restype = ctypes.c_int
@@ -116,6 +120,42 @@ def verify_rows(inp, rows: Optional[Sequence[int]] = None,
 def verify(inp, threads: int = 0, mutant: int = 0):
     """All output rows: (out [total_q, H, 512], lse [total_q, H])."""
     out, lse = verify_rows(inp, None, threads=threads, mutant=mutant)
+    return out.reshape(inp.total_q, inp.num_heads, -1), lse.reshape(inp.total_q, inp.num_heads)
+
+
+def verify_sparse_rows(inp, topk_idx, rows: Optional[Sequence[int]] = None, threads: int = 0,
+                       mutant: int = 0, d_latent: int = 512) -> Tuple[np.ndarray, np.ndarray]:
+    """Sparse (top-k) variant: tree token g sees the prefix positions listed in
+    topk_idx[g] (int32 [total_q, topk], -1 = unused slot, one key per slot) and
+    its ancestor-or-self tree tokens.  Returns (out [n, d_latent], lse [n])."""
+    lib = load(mutant)
+    H = inp.num_heads
+    if rows is None:
+        rows = np.arange(inp.total_q * H, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    assert idx.ndim == 2 and idx.shape[0] == inp.total_q
+    out = np.zeros((n, d_latent), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    arrs = [np.ascontiguousarray(a) for a in (inp.q_lat, inp.q_rope, inp.kv_cache)]
+    ints = [np.ascontiguousarray(a, dtype=np.int32) for a in
+            (inp.block_table, inp.seq_lens, inp.tree_parent, inp.n_tree)]
+    st = lib.mla_oracle_verify_sparse_rows(
+        _p(arrs[0], ctypes.c_uint16), _p(arrs[1], ctypes.c_uint16), _p(arrs[2], ctypes.c_uint16),
+        _p(ints[0], ctypes.c_int32), _p(ints[1], ctypes.c_int32), _p(ints[2], ctypes.c_int32),
+        _p(ints[3], ctypes.c_int32), _p(idx, ctypes.c_int32), idx.shape[1], float(inp.scale), inp.batch,
+        inp.total_q, H, d_latent, inp.q_rope.shape[-1], inp.page_size, inp.block_table.shape[1],
+        inp.kv_cache.shape[0], _p(rows, ctypes.c_int64), n, _p(out, ctypes.c_double),
+        _p(lse, ctypes.c_double), int(threads))
+    if st != 0:
+        raise OracleError(st)
+    return out, lse
+
+
+def verify_sparse(inp, topk_idx, threads: int = 0, mutant: int = 0):
+    """All output rows of the sparse variant: (out [total_q, H, 512], lse [total_q, H])."""
+    out, lse = verify_sparse_rows(inp, topk_idx, None, threads=threads, mutant=mutant)
     return out.reshape(inp.total_q, inp.num_heads, -1), lse.reshape(inp.total_q, inp.num_heads)
 
 

@@ -28,9 +28,18 @@
  * split-KV partial of that range).  mla_oracle_combine merges such partials
  * with the log-sum-exp weights of flash-decoding.
  *
+ * Sparse (top-k) variant, mla_oracle_verify_sparse_rows (page "The SMEM
+ * Ceiling", section "The Problem Space": during decode each token attends to
+ * a sparse set of previous tokens chosen by a top-k index selection): tree
+ * token g carries topk slots topk_idx[g][0..topk); each slot holding a prefix
+ * position t in [0, P) contributes that key once (a position listed twice
+ * counts twice), -1 marks an unused slot.  The prefix part of V is replaced by
+ * these slots; the ancestor-or-self tree keys stay visible as above.
+ *
  * Returns 0 on success; 1 for an invalid argument; 6 for an invalid draft
  * tree or length (parent outside [-1, i), n_tree > seq_len, negative sizes);
- * 7 for a block-table entry outside [0, num_pages).
+ * 7 for a block-table entry outside [0, num_pages); 9 for a top-k slot that is
+ * neither -1 nor a prefix position.
  */
 #include <math.h>
 #include <pthread.h>
@@ -43,11 +52,13 @@
 #define ORACLE_MUTANT 0 /* non-zero only in deliberately broken test builds */
 #endif
 
-enum { OR_OK = 0, OR_BAD_ARG = 1, OR_BAD_TREE = 6, OR_BAD_BLOCK = 7 };
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_BAD_TREE = 6, OR_BAD_BLOCK = 7, OR_BAD_INDEX = 9 };
 
 typedef struct {
     const uint16_t *q_lat, *q_rope, *kv;
     const int32_t *block_table, *seq_lens, *parent, *n_tree;
+    const int32_t *topk_idx;  /* [total_q][topk] or NULL (dense: the whole prefix) */
+    int64_t topk;
     int64_t batch, total_q, heads, dl, dr, page, max_pages, num_pages;
     double scale;
     int64_t *q_off;   /* [batch + 1] first q index of each request */
@@ -87,8 +98,21 @@ static int one_row(const problem_t *p, int64_t g, int64_t h, int64_t k0, int64_t
     const int64_t D = p->dl + p->dr;
     int64_t n = 0;
 
-    /* the whole prefix is visible */
-    for (int64_t t = (k0 > 0 ? k0 : 0); t < P && t < k1; ++t) keys[n++] = t;
+    if (p->topk > 0) {
+        /* the listed prefix positions, one key per slot */
+        for (int64_t sl = 0; sl < p->topk; ++sl) {
+            int64_t t = p->topk_idx[g * p->topk + sl];
+#if ORACLE_MUTANT == 11
+            if (t >= 0 && t + 1 < P) t += 1;        /* every listed position off by one */
+#elif ORACLE_MUTANT == 12
+            if (t < 0 && P > 0) t = 0;              /* unused slots attend to position 0 */
+#endif
+            if (t >= 0 && t >= k0 && t < k1) keys[n++] = t;
+        }
+    } else {
+        /* the whole prefix is visible */
+        for (int64_t t = (k0 > 0 ? k0 : 0); t < P && t < k1; ++t) keys[n++] = t;
+    }
     /* ancestor-or-self walk up the parent array */
 #if ORACLE_MUTANT == 2
     int64_t j = p->parent[base + i];      /* forgets the node itself */
@@ -177,6 +201,7 @@ static void *worker(void *arg)
     int64_t maxlen = 1;
     for (int64_t b = 0; b < p->batch; ++b)
         if (p->seq_lens[b] > maxlen) maxlen = p->seq_lens[b];
+    if (p->topk + 64 > maxlen) maxlen = p->topk + 64;   /* slots may repeat positions */
     int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(maxlen + 1));
     double *score = (double *)malloc(sizeof(double) * (size_t)(maxlen + 1));
     if (!keys || !score) {
@@ -218,6 +243,15 @@ static int prepare(problem_t *p)
             int64_t up = p->parent[p->q_off[b] + j];
             if (up < -1 || up >= j) return OR_BAD_TREE;
         }
+    if (p->topk > 0)
+        for (int64_t b = 0; b < p->batch; ++b) {
+            const int64_t P = p->seq_lens[b] - p->n_tree[b];
+            for (int64_t g = p->q_off[b]; g < p->q_off[b + 1]; ++g)
+                for (int64_t sl = 0; sl < p->topk; ++sl) {
+                    int64_t t = p->topk_idx[g * p->topk + sl];
+                    if (t < -1 || t >= P) return OR_BAD_INDEX;
+                }
+        }
     for (int64_t b = 0; b < p->batch; ++b) {
         int64_t pages = (p->seq_lens[b] + p->page - 1) / p->page;
         for (int64_t k = 0; k < pages; ++k) {
@@ -254,14 +288,14 @@ int mla_oracle_check(const int32_t *block_table, const int32_t *seq_lens,
     return st;
 }
 
-int mla_oracle_verify_rows(const uint16_t *q_lat, const uint16_t *q_rope, const uint16_t *kv_cache,
+static int verify_rows(const uint16_t *q_lat, const uint16_t *q_rope, const uint16_t *kv_cache,
                            const int32_t *block_table, const int32_t *seq_lens,
-                           const int32_t *tree_parent, const int32_t *n_tree, double scale,
-                           int64_t batch, int64_t total_q, int64_t num_heads, int64_t d_latent,
-                           int64_t d_rope, int64_t page_size, int64_t max_pages_per_seq,
-                           int64_t num_pages, const int64_t *rows, int64_t n_rows,
-                           int64_t key_begin, int64_t key_end, double *out, double *lse,
-                           int threads)
+                       const int32_t *tree_parent, const int32_t *n_tree, double scale,
+                       int64_t batch, int64_t total_q, int64_t num_heads, int64_t d_latent,
+                       int64_t d_rope, int64_t page_size, int64_t max_pages_per_seq,
+                       int64_t num_pages, const int64_t *rows, int64_t n_rows,
+                       int64_t key_begin, int64_t key_end, double *out, double *lse,
+                       int threads, const int32_t *topk_idx, int64_t topk)
 {
     problem_t p;
     memset(&p, 0, sizeof p);
@@ -281,6 +315,9 @@ int mla_oracle_verify_rows(const uint16_t *q_lat, const uint16_t *q_rope, const 
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
     p.scale = scale;
+    p.topk_idx = topk_idx;
+    p.topk = topk;
+    if (topk < 0 || (topk > 0 && !topk_idx)) return OR_BAD_ARG;
     if (n_rows < 0 || (n_rows > 0 && (!rows || !out || !lse))) return OR_BAD_ARG;
     p.q_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(batch + 1));
     p.q_req = (int64_t *)malloc(sizeof(int64_t) * (size_t)(total_q + 1));
@@ -304,6 +341,35 @@ int mla_oracle_verify_rows(const uint16_t *q_lat, const uint16_t *q_rope, const 
     free(p.q_off);
     free(p.q_req);
     return st;
+}
+
+int mla_oracle_verify_rows(const uint16_t *q_lat, const uint16_t *q_rope, const uint16_t *kv_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *tree_parent, const int32_t *n_tree, double scale,
+                           int64_t batch, int64_t total_q, int64_t num_heads, int64_t d_latent,
+                           int64_t d_rope, int64_t page_size, int64_t max_pages_per_seq,
+                           int64_t num_pages, const int64_t *rows, int64_t n_rows,
+                           int64_t key_begin, int64_t key_end, double *out, double *lse,
+                           int threads)
+{
+    return verify_rows(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, batch,
+                       total_q, num_heads, d_latent, d_rope, page_size, max_pages_per_seq, num_pages, rows,
+                       n_rows, key_begin, key_end, out, lse, threads, NULL, 0);
+}
+
+int mla_oracle_verify_sparse_rows(const uint16_t *q_lat, const uint16_t *q_rope, const uint16_t *kv_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  const int32_t *tree_parent, const int32_t *n_tree,
+                                  const int32_t *topk_idx, int64_t topk, double scale,
+                                  int64_t batch, int64_t total_q, int64_t num_heads, int64_t d_latent,
+                                  int64_t d_rope, int64_t page_size, int64_t max_pages_per_seq,
+                                  int64_t num_pages, const int64_t *rows, int64_t n_rows,
+                                  double *out, double *lse, int threads)
+{
+    if (topk <= 0) return OR_BAD_ARG;
+    return verify_rows(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, batch,
+                       total_q, num_heads, d_latent, d_rope, page_size, max_pages_per_seq, num_pages, rows,
+                       n_rows, 0, INT64_MAX, out, lse, threads, topk_idx, topk);
 }
 
 /* Flash-decoding merge of split partials: part_out [n_splits][rows][dv] holds

@@ -67,3 +67,34 @@ def brute(inp, d_latent=512):
                     out[off + i, h, d] = math.fsum(w * kv[t, d] for w, t in zip(e, vis)) / z
         off += T
     return out, lse
+
+
+def brute_sparse(inp, topk_idx, d_latent=512):
+    """Sparse variant: the visible multiset of tree token g is its listed prefix
+    positions (one key per non-negative slot) plus its ancestor-or-self tree keys."""
+    H = inp.num_heads
+    out = np.zeros((inp.total_q, H, d_latent))
+    lse = np.zeros((inp.total_q, H))
+    ql = bf16_bits_to_f64(inp.q_lat)
+    qr = bf16_bits_to_f64(inp.q_rope)
+    dr = qr.shape[-1]
+    off = 0
+    for b in range(inp.batch):
+        T = int(inp.n_tree[b])
+        P = int(inp.seq_lens[b]) - T
+        par = [int(x) for x in inp.tree_parent[off:off + T]]
+        A = ancestor_matrix(par)
+        kv = logical_kv(inp, b)
+        for i in range(T):
+            vis = [int(t) for t in topk_idx[off + i] if t >= 0] + [P + j for j in range(T) if A[i][j]]
+            for h in range(H):
+                q = list(ql[off + i, h]) + list(qr[off + i, h])
+                s = [inp.scale * math.fsum(a * c for a, c in zip(q, list(kv[t, :d_latent + dr]))) for t in vis]
+                e = [math.exp(x) for x in s]
+                z = math.fsum(e)
+                lse[off + i, h] = math.log(z)
+                for d in range(d_latent):
+                    out[off + i, h, d] = math.fsum(w * kv[t, d] for w, t in zip(e, vis)) / z
+        off += T
+    return out, lse
+

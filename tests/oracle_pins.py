@@ -266,9 +266,66 @@ def pin_validation(mutant=0):
     assert oracle.check(bad, mutant=mutant) == 7
 
 
+def _sparse_check(got, want, tol=1e-12):
+    assert np.max(np.abs(got[0] - want[0])) <= tol and np.max(np.abs(got[1] - want[1])) <= tol
+
+
+def pin_sparse_brute(mutant=0):
+    """Sparse variant against the brute-force multiset definition (unused and repeated slots)."""
+    from brute import brute_sparse
+    for seed in range(3):
+        inp = _tiny(seed, max_p=9)
+        idx = I.topk_indices(inp, 6, seed=seed, unused_frac=0.25, duplicates=True)
+        _sparse_check(oracle.verify_sparse(inp, idx, mutant=mutant), brute_sparse(inp, idx), 1e-11)
+
+
+def pin_sparse_full_list_is_dense(mutant=0):
+    """Listing every prefix position (any order, -1 padding) gives the dense result."""
+    inp = _tiny(5, max_p=12)
+    P = (inp.seq_lens - inp.n_tree).astype(int)
+    topk = int(P.max()) + 3
+    idx = I.topk_indices(inp, topk, seed=5)
+    assert all(sorted(int(t) for t in idx[g] if t >= 0) == list(range(P[b]))
+               for b in range(inp.batch) for g in range(int(inp.q_offsets[b]), int(inp.q_offsets[b + 1])))
+    _sparse_check(oracle.verify_sparse(inp, idx, mutant=mutant), oracle.verify(inp, mutant=mutant))
+
+
+def pin_sparse_repeated_slot_closed_form(mutant=0):
+    """One root, slots [t, t]: weights 2e^{s_t} : e^{s_root}, so lse = ln(2e^{s_t} + e^{s_root})."""
+    inp = I.make_inputs([7], [1], tree_kind="forest", page_size=2, seed=4, stream=20, num_heads=1)
+    t = 3
+    idx = np.array([[t, -1, t]], np.int32)
+    out, lse = oracle.verify_sparse(inp, idx, mutant=mutant)
+    from brute import logical_kv
+    kv = logical_kv(inp, 0)
+    q = np.concatenate([I.bf16_bits_to_f64(inp.q_lat[0, 0]), I.bf16_bits_to_f64(inp.q_rope[0, 0])])
+    s_t = inp.scale * math.fsum(q * kv[t, :576])
+    s_r = inp.scale * math.fsum(q * kv[7, :576])
+    z = 2 * math.exp(s_t) + math.exp(s_r)
+    assert abs(lse[0, 0] - math.log(z)) < 1e-12
+    want = (2 * math.exp(s_t) * kv[t, :512] + math.exp(s_r) * kv[7, :512]) / z
+    assert np.max(np.abs(out[0, 0] - want)) < 1e-12
+
+
+def pin_sparse_validation(mutant=0):
+    """A slot that is neither -1 nor a prefix position is rejected (status 9)."""
+    inp = _tiny(6, max_p=9)
+    P0 = int(inp.seq_lens[0] - inp.n_tree[0])
+    for bad in (P0, -2, 1 << 20):
+        idx = I.topk_indices(inp, 4, seed=6)
+        idx[0, 1] = bad
+        try:
+            oracle.verify_sparse(inp, idx, mutant=mutant)
+        except oracle.OracleError as e:
+            assert e.status == 9
+        else:
+            raise AssertionError(f"slot {bad} accepted")
+
+
 ALL_PINS = [pin_brute, pin_single_key, pin_uniform, pin_chain_causal, pin_split,
             pin_combine_closed_form, pin_permutation, pin_torch_library, pin_golden_hand,
-            pin_validation]
+            pin_validation, pin_sparse_brute, pin_sparse_full_list_is_dense,
+            pin_sparse_repeated_slot_closed_form, pin_sparse_validation]
 MUTANTS = {
     1: "rope term dropped from the score",
     2: "node does not see itself",
@@ -280,4 +337,6 @@ MUTANTS = {
     8: "V read at the wrong column offset",
     9: "tree keys shifted by one position",
     10: "combine uses the max instead of the log-sum-exp",
+    11: "every listed top-k position off by one",
+    12: "unused top-k slots attend to position 0",
 }

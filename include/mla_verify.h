@@ -51,7 +51,8 @@ typedef enum {
     MLA_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (status word)  */
     MLA_ERR_BAD_TREE = 6,     /* parent outside [-1, i), n_tree > seq_len, sums    */
     MLA_ERR_BAD_BLOCK = 7,    /* block-table entry outside [0, num_pages)          */
-    MLA_ERR_NOT_INITIALIZED = 8 /* mla_init() has not run on the current device    */
+    MLA_ERR_NOT_INITIALIZED = 8, /* mla_init() has not run on the current device   */
+    MLA_ERR_BAD_INDEX = 9     /* sparse variant: a top-k slot outside {-1} u [0, prefix) */
 } mla_status;
 
 #define MLA_NUM_HEADS 64
@@ -59,6 +60,7 @@ typedef enum {
 #define MLA_D_ROPE 64
 #define MLA_MAX_TREE 64
 #define MLA_MAX_SPLITS 64
+#define MLA_MAX_TOPK 2048
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int mla_version(void);
@@ -150,6 +152,37 @@ int mla_verify_attn(const void *q_lat, const void *q_rope, const void *kv_cache,
  */
 int mla_split_combine(const float *part_out, const float *part_lse, int num_splits, int rows,
                       float *out, float *lse, cudaStream_t stream);
+
+/*
+ * Sparse (top-k) tree verification ("The SMEM Ceiling", section "The Problem
+ * Space": during decode each token attends to a sparse set of previous tokens
+ * chosen by a top-k index selection).  Arguments as for mla_verify_attn, plus
+ *  topk_idx  device int32 [total_q, topk]: for each tree token, the prefix
+ *            positions (0 <= t < seq_len - n_tree of its request) it attends
+ *            to, in any order; -1 marks an unused slot.  Each listed slot is
+ *            one key (a position listed twice counts twice).
+ *  topk      1 <= topk <= MLA_MAX_TOPK (the pages' kernel uses 512).
+ * Token i of request b then sees its listed prefix positions and its
+ * ancestor-or-self tree tokens, in all heads: out / lse as for
+ * mla_verify_attn over that key set.  A slot outside {-1} u [0, prefix) sets
+ * status bit 1 << MLA_ERR_BAD_INDEX and the request's rows are written as
+ * out = 0, lse = -inf.  The two tree tokens of a 128-row tile share one key
+ * stream (their slot lists one after the other), so the tensor work per tile
+ * is twice the visible work.
+ * mla_verify_sparse_num_splits / mla_verify_sparse_workspace_size: as the
+ * dense ones, for `topk` instead of max_seq_len.
+ */
+int mla_verify_sparse_num_splits(int batch, int total_q, int max_tree, int topk, int num_heads,
+                                 int requested);
+size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, int topk,
+                                        int num_heads, int num_splits);
+int mla_verify_sparse_attn(const void *q_lat, const void *q_rope, const void *kv_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *tree_parent, const int32_t *n_tree,
+                           const int32_t *topk_idx, int topk, float scale, float *out, float *lse,
+                           cudaStream_t stream, int batch, int total_q, int max_tree, int max_seq_len,
+                           int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                           int num_splits, void *workspace, size_t workspace_bytes);
 
 /*
  * mla_verify_attn for callers that cannot allocate device memory: the page

@@ -24,17 +24,20 @@ MLA_ERR_TIMEOUT = 5
 MLA_ERR_BAD_TREE = 6
 MLA_ERR_BAD_BLOCK = 7
 MLA_ERR_NOT_INITIALIZED = 8
+MLA_ERR_BAD_INDEX = 9
 
 NUM_HEADS = 64
 D_LATENT = 512
 D_ROPE = 64
 MAX_TREE = 64
 MAX_SPLITS = 64
+MAX_TOPK = 2048
 
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
             "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc",
-            "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept")
+            "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept",
+            "mla_verify_sparse_num_splits", "mla_verify_sparse_workspace_size", "mla_verify_sparse_attn")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -79,6 +82,13 @@ def lib() -> ctypes.CDLL:
         L.mla_set_profile_events.argtypes = [vp, vp]
         L.mla_read_status.restype = i32
         L.mla_read_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.mla_verify_sparse_num_splits.restype = i32
+        L.mla_verify_sparse_num_splits.argtypes = [i32] * 6
+        L.mla_verify_sparse_workspace_size.restype = sz
+        L.mla_verify_sparse_workspace_size.argtypes = [i32] * 6
+        L.mla_verify_sparse_attn.restype = i32
+        L.mla_verify_sparse_attn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, vp, vp,
+                                             i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz]
         L.mla_tree_kv_workspace_size.restype = sz
         L.mla_tree_kv_workspace_size.argtypes = []
         L.mla_tree_kv_append.restype = i32
@@ -146,6 +156,27 @@ def split_combine(part_out, part_lse, num_splits, rows, out, lse, stream) -> int
 def set_profile_events(begin, end) -> None:
     """Record CUDA events (raw cudaEvent_t handles) around the fused verify kernel."""
     check(lib().mla_set_profile_events(begin, end), "mla_set_profile_events")
+
+
+def sparse_num_splits(batch, total_q, max_tree, topk, num_heads=NUM_HEADS, requested=0) -> int:
+    s = lib().mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, requested)
+    if s <= 0:
+        raise MlaError(-s, "mla_verify_sparse_num_splits")
+    return int(s)
+
+
+def sparse_workspace_size(batch, total_q, max_tree, topk, num_heads=NUM_HEADS, splits=0) -> int:
+    return int(lib().mla_verify_sparse_workspace_size(batch, total_q, max_tree, topk, num_heads, splits))
+
+
+def verify_sparse_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, topk_idx, topk,
+                       scale, out, lse, stream, batch, total_q, max_tree, max_seq_len, num_heads, page_size,
+                       num_pages, max_pages_per_seq, num_splits, workspace, workspace_bytes) -> int:
+    """Raw call of the sparse (top-k) variant; returns the mla_status code."""
+    return int(lib().mla_verify_sparse_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree,
+                                            topk_idx, topk, float(scale), out, lse, stream, batch, total_q,
+                                            max_tree, max_seq_len, num_heads, page_size, num_pages,
+                                            max_pages_per_seq, num_splits, workspace, workspace_bytes))
 
 
 def tree_kv_workspace_size() -> int:
@@ -257,3 +288,29 @@ def accept_path(db: "DeviceBatch", accept_len, accept_idx, new_seq_lens=None, wo
                          inp.total_q, inp.page_size, inp.num_pages, inp.max_pages_per_seq,
                          workspace.data_ptr(), workspace.numel()), "mla_tree_kv_accept")
     return new_seq_lens, workspace
+
+
+def verify_sparse(db: "DeviceBatch", topk_idx, num_splits_req: int = 0, out=None, lse=None, workspace=None,
+                  stream=None):
+    """Run mla_verify_sparse_attn; topk_idx is a device int32 tensor [total_q, topk].
+    Returns (out, lse, workspace)."""
+    import torch
+    inp = db.inp
+    topk = int(topk_idx.shape[1])
+    if out is None:
+        out = torch.empty((inp.total_q, inp.num_heads, D_LATENT), dtype=torch.float32, device=db.device)
+    if lse is None:
+        lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=db.device)
+    need = sparse_workspace_size(inp.batch, inp.total_q, inp.max_tree, topk, inp.num_heads, num_splits_req)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=db.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(db.device)
+    check(verify_sparse_attn(db.q_lat.data_ptr(), db.q_rope.data_ptr(), db.kv_cache.data_ptr(),
+                             db.block_table.data_ptr(), db.seq_lens.data_ptr(), db.tree_parent.data_ptr(),
+                             db.n_tree.data_ptr(), topk_idx.data_ptr(), topk, inp.scale, out.data_ptr(),
+                             lse.data_ptr(), stream.cuda_stream, inp.batch, inp.total_q, inp.max_tree,
+                             inp.max_seq_len, inp.num_heads, inp.page_size, inp.num_pages, inp.max_pages_per_seq,
+                             num_splits_req, workspace.data_ptr(), workspace.numel()), "mla_verify_sparse_attn")
+    return out, lse, workspace
+

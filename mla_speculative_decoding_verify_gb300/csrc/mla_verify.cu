@@ -96,10 +96,10 @@ double model_time(long long units_per_split, int tiles, int splits, int pairs, l
     return t;
 }
 
-int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
+// Split count for requests of up to `tiles` KV tiles per row tile.
+int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
     const long long items_bound = std::min<long long>(static_cast<long long>(batch) * ((max_tree + 1) / 2),
                                                       (static_cast<long long>(total_q) + batch) / 2);
-    const int tiles = (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
     const int pairs = sm_count_of_current() / 2;
     const long long rows = static_cast<long long>(total_q) * MLA_NUM_HEADS;
     const int max_s = std::max(1, std::min(MLA_MAX_SPLITS, tiles / 16));
@@ -114,6 +114,13 @@ int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
     }
     return best;
 }
+
+int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
+    return choose_splits_tiles(batch, total_q, max_tree, (max_seq_len + mla::kBlockN - 1) / mla::kBlockN);
+}
+
+// KV tiles of a sparse row tile: two tokens' slot lists, then the tree keys.
+int sparse_tiles(int topk) { return 2 * ((topk + mla::kBlockN - 1) / mla::kBlockN) + 1; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -159,6 +166,7 @@ const char* mla_error_string(int status) {
         case MLA_ERR_BAD_TREE: return "invalid draft tree or lengths";
         case MLA_ERR_BAD_BLOCK: return "block-table entry out of range";
         case MLA_ERR_NOT_INITIALIZED: return "mla_init has not run on this device";
+        case MLA_ERR_BAD_INDEX: return "a top-k slot is neither -1 nor a prefix position";
         default: return "unknown status";
     }
 }
@@ -183,7 +191,10 @@ int mla_init(int device) {
     if (cudaFuncSetAttribute(mla::mla_tree_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(mla::kAcceptSmemBytes)) != cudaSuccess)
         return MLA_ERR_CUDA;
-    if (cudaFuncSetAttribute(mla::mla_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mla::mla_verify_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaFuncSetAttribute(mla::mla_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
         return MLA_ERR_CUDA;
     g_dev[device].sm_count = prop.multiProcessorCount;
@@ -205,11 +216,13 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
     return make_layout(batch, total_q, s).total;
 }
 
-int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
-                    const int32_t* seq_lens, const int32_t* tree_parent, const int32_t* n_tree, float scale,
-                    float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
-                    int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
-                    int num_splits, void* workspace, size_t workspace_bytes) {
+// Both entry points: topk == 0 is the dense verify, topk > 0 the sparse variant.
+static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* tree_parent, const int32_t* n_tree, float scale,
+                       float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
+                       int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                       int num_splits, void* workspace, size_t workspace_bytes, const int32_t* topk_idx,
+                       int topk) {
     // ---- host-checkable arguments ----
     if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
         num_splits < 0 || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
@@ -226,7 +239,8 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
     if (num_pages == 0 || max_pages_per_seq == 0) return MLA_ERR_INVALID_ARG;
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MLA_ERR_NOT_INITIALIZED;
-    const int splits = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
+    const int splits = topk > 0 ? mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits)
+                                : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (splits <= 0) return MLA_ERR_INVALID_ARG;
     const Layout lay = make_layout(batch, total_q, splits);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -266,6 +280,8 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
     pp.max_pages = max_pages_per_seq;
     pp.num_pages = num_pages;
     pp.max_items = lay.max_items;
+    pp.topk_idx = topk_idx;
+    pp.topk = topk;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
@@ -295,9 +311,15 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
     vp.max_items = lay.max_items;
     vp.scale_log2 = scale * 1.4426950408889634f;
     vp.timeout_ns = kDefaultTimeoutNs;
+    vp.topk_idx = topk_idx;
+    vp.kv_bytes = static_cast<const uint8_t*>(kv_cache);
+    vp.topk = topk;
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
     if (g_prof_begin && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
-    mla::mla_verify_kernel<<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    if (topk > 0)
+        mla::mla_verify_kernel<true><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    else
+        mla::mla_verify_kernel<false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (g_prof_end && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
@@ -306,6 +328,44 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
         return launch_combine(part_out, part_lse, splits, static_cast<long long>(total_q) * MLA_NUM_HEADS, out, lse,
                               stream);
     return MLA_OK;
+}
+
+int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, const int32_t* tree_parent, const int32_t* n_tree, float scale,
+                    float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
+                    int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                    int num_splits, void* workspace, size_t workspace_bytes) {
+    return verify_impl(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, out, lse, stream,
+                       batch, total_q, max_tree, max_seq_len, num_heads, page_size, num_pages, max_pages_per_seq,
+                       num_splits, workspace, workspace_bytes, nullptr, 0);
+}
+
+int mla_verify_sparse_num_splits(int batch, int total_q, int max_tree, int topk, int num_heads, int requested) {
+    if (batch < 0 || total_q < 0 || max_tree < 0 || requested < 0 || topk < 1) return -MLA_ERR_INVALID_ARG;
+    if (num_heads != MLA_NUM_HEADS || topk > MLA_MAX_TOPK) return -MLA_ERR_UNSUPPORTED;
+    if (requested > 0) return std::min(requested, MLA_MAX_SPLITS);
+    return choose_splits_tiles(batch, total_q, max_tree, sparse_tiles(topk));
+}
+
+size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, int topk, int num_heads,
+                                        int num_splits) {
+    const int s = mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits);
+    if (s <= 0) return 0;
+    return make_layout(batch, total_q, s).total;
+}
+
+int mla_verify_sparse_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, const int32_t* tree_parent, const int32_t* n_tree,
+                           const int32_t* topk_idx, int topk, float scale, float* out, float* lse,
+                           cudaStream_t stream, int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
+                           int page_size, int num_pages, int max_pages_per_seq, int num_splits, void* workspace,
+                           size_t workspace_bytes) {
+    if (topk < 1) return MLA_ERR_INVALID_ARG;
+    if (topk > MLA_MAX_TOPK) return MLA_ERR_UNSUPPORTED;
+    if (batch > 0 && total_q > 0 && !topk_idx) return MLA_ERR_INVALID_ARG;
+    return verify_impl(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, out, lse, stream,
+                       batch, total_q, max_tree, max_seq_len, num_heads, page_size, num_pages, max_pages_per_seq,
+                       num_splits, workspace, workspace_bytes, topk_idx, topk);
 }
 
 int mla_split_combine(const float* part_out, const float* part_lse, int num_splits, int rows, float* out, float* lse,

@@ -31,6 +31,8 @@ struct PrepParams {
     int32_t* item_count;         // [1]
     int* status;                 // [1]
     int batch, total_q, page_size, max_pages, num_pages, max_items;
+    const int32_t* topk_idx;     // sparse variant: [total_q, topk], else null
+    int topk;
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
@@ -110,12 +112,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
                 }
             }
         }
+        // sparse variant: every slot is -1 or a prefix position
+        bool bad_index = false;
+        if (shape_ok && p.topk > 0) {
+            const long long n = static_cast<long long>(T) * p.topk;
+            const int32_t* idx = p.topk_idx + static_cast<long long>(base) * p.topk;
+            for (long long k = lane; k < n; k += 32) {
+                const int v = __ldg(idx + k);
+                bad_index |= v < -1 || v >= L - T;
+            }
+        }
         bad_parent = __any_sync(0xffffffffu, bad_parent);
         bad_block = __any_sync(0xffffffffu, bad_block);
-        const bool all_ok = shape_ok && !bad_parent && !bad_block;
+        bad_index = __any_sync(0xffffffffu, bad_index);
+        const bool all_ok = shape_ok && !bad_parent && !bad_block && !bad_index;
         if (lane == 0) {
             p.req_state[b] = shape_ok ? (all_ok ? 0 : 1) : 2;  // 2: outputs not written at all
-            const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0);
+            const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0) |
+                             (bad_index ? kStatusBadIndex : 0);
             if (bits) atomicOr(p.status, bits);
         }
         __syncwarp();

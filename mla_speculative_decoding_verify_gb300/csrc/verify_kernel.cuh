@@ -21,6 +21,14 @@
 // tile while the copy is in flight; an S buffer is therefore free again right
 // after it was read, and the QK issuer runs ahead, bounded by the KV ring.  A
 // second MMA warp issues PV as soon as a tile's P is in shared memory.
+// Sparse (top-k) variant (kSparse = true; page "The SMEM Ceiling", section
+// "The Problem Space": each token attends to a top-k selected set of earlier
+// tokens): tree token g sees the prefix positions listed in its topk slots and
+// its ancestor-or-self tree tokens.  A row tile's key sequence is token 0's
+// slots, then token 1's slots, then the tree keys; rows see only their own
+// token's slots.  Warp 0 gathers the rows with per-thread 16-byte async
+// copies into the same swizzled stage layout (empty slots are zero-filled) and
+// records which of the tile's 64 slots are real.
 // TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
 #pragma once
 
@@ -74,6 +82,7 @@ constexpr float kLowPartShare = 1.0f / 16.0f;
 constexpr int kStatusTimeout = 1 << 5;
 constexpr int kStatusBadTree = 1 << 6;
 constexpr int kStatusBadBlock = 1 << 7;
+constexpr int kStatusBadIndex = 1 << 9;
 
 struct VerifyParams {
     const uint16_t* q_lat;      // [total_q, 64, 512]
@@ -94,6 +103,10 @@ struct VerifyParams {
     int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
     float scale_log2;           // softmax scale * log2(e)
     uint64_t timeout_ns;
+    // sparse variant only
+    const int32_t* topk_idx;    // [total_q, topk] prefix positions, -1 = unused slot
+    const uint8_t* kv_bytes;    // the cache as bytes, rows of 1152
+    int topk;
 };
 
 struct Ctrl {
@@ -114,6 +127,7 @@ struct Ctrl {
     int abort;
     int lo_flag[2];
     int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
+    uint64_t slot_mask[kStages];  // sparse: bit k set if key k of the stage's tile is a real slot
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -125,6 +139,22 @@ __device__ __forceinline__ void split_range(int n, int s, int S, int& t0, int& t
     t1 = static_cast<int>((static_cast<long long>(n) * (s + 1)) / S);
 }
 
+// Sparse key sequence of a row tile: tiles [0, nA) hold token 0's slots, [nA, nA + nB)
+// token 1's, the rest the tree keys.  kind 0 / 1: slots of that token; kind 2: tree keys.
+__device__ __forceinline__ void sparse_segment(int j, int nA, int nB, int& kind, int& base) {
+    if (j < nA) {
+        kind = 0;
+        base = j * kBlockN;
+    } else if (j < nA + nB) {
+        kind = 1;
+        base = (j - nA) * kBlockN;
+    } else {
+        kind = 2;
+        base = (j - nA - nB) * kBlockN;
+    }
+}
+
+template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap map_lat,
                   const __grid_constant__ CUtensorMap map_rope) {
@@ -150,7 +180,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int qbase = __ldg(p.q_off + b) + kTokensPerTile * tile;
     const int ntok = min(kTokensPerTile, T - kTokensPerTile * tile);
     const bool bad = __ldg(p.req_state + b) != 0;
-    const int n_kv_tiles = bad ? 0 : (L + kBlockN - 1) / kBlockN;
+    int nA = 0, nB = 0;
+    if constexpr (kSparse) {
+        nA = (p.topk + kBlockN - 1) / kBlockN;
+        nB = ntok > 1 ? nA : 0;
+    }
+    const int n_kv_tiles =
+        bad ? 0 : (kSparse ? nA + nB + (T + kBlockN - 1) / kBlockN : (L + kBlockN - 1) / kBlockN);
     int t0, t1;
     split_range(n_kv_tiles, split, p.num_splits, t0, t1);
     const int n = t1 - t0;
@@ -185,7 +221,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // ---- set-up ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->kv_full[s], 1);
+            mbar_init(&ctl->kv_full[s], kSparse ? 32 : 1);  // sparse: one arrival per producer lane
             mbar_init(&ctl->kv_empty[s], 1);
             mbar_init(&ctl->kv_fixed[s], 1);
         }
@@ -225,7 +261,89 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
     const uint32_t p_addr = smem_u32(smem + kOffP);
 
-    if (warp == 0) {
+    if (warp == 0 && kSparse) {
+        // ================= gather producer (sparse) =================
+        // Lane l fills keys l and l + 32 of each tile: this CTA's latent half
+        // (512 B as 4 x 8 16-byte units, 128B swizzle) and rope half (64 B, 64B
+        // swizzle).  Copies of tile jj are released to QK after tile jj + 1 was
+        // issued (cp.async groups, then a proxy fence and one arrival per lane).
+        bool ok = true;
+        int issued = 0;
+        for (int jj = 0; jj < n && ok; ++jj) {
+            const int st = jj % kStages;
+            if (jj >= kStages) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
+                if (!ok) break;
+            }
+            int kind, base;
+            sparse_segment(t0 + jj, nA, nB, kind, base);
+            const uint32_t sb = stage0 + st * kStageBytes;
+            bool valid[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int key = lane + 32 * h;
+                int pos = -1;
+                if (kind == 2) {
+                    if (base + key < T) pos = P + base + key;
+                } else if (base + key < p.topk) {
+                    pos = __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key);
+                    if (pos >= P) pos = -1;   // rejected by the prep kernel; never read
+                }
+                long long row = -1;
+                if (pos >= 0) {
+                    const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + pos / p.page_size);
+                    if (page >= 0 && page < p.num_pages) {
+                        row = static_cast<long long>(page) * p.page_size + pos % p.page_size;
+                    } else {
+                        raise_status(p.status, kStatusBadBlock);
+                    }
+                }
+                valid[h] = row >= 0;
+                const uint32_t lat = sb + key * 128;
+                const uint32_t rope = sb + 4 * kChunkBytes + key * 64;
+                if (valid[h]) {
+                    const uint8_t* src = p.kv_bytes + row * (kDqk * 2);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            cp_async_16(lat + ch * kChunkBytes + ((u ^ (key & 7)) << 4),
+                                        src + kDLatentHalf * 2 * c + 128 * ch + 16 * u);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        cp_async_16(rope + ((u ^ ((key >> 1) & 3)) << 4), src + kDLatent * 2 + kDRopeHalf * 2 * c + 16 * u);
+                } else {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) st_shared_v4(lat + ch * kChunkBytes + (u << 4), z.x, z.y, z.z, z.w);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) st_shared_v4(rope + (u << 4), z.x, z.y, z.z, z.w);
+                }
+            }
+            const uint32_t lo_bits = __ballot_sync(0xffffffffu, valid[0]);
+            const uint32_t hi_bits = __ballot_sync(0xffffffffu, valid[1]);
+            if (lane == 0) ctl->slot_mask[st] = (static_cast<uint64_t>(hi_bits) << 32) | lo_bits;
+            cp_async_commit();
+            ++issued;
+            if (jj >= 1) {
+                cp_async_wait<1>();        // tile jj - 1 has landed
+                fence_proxy_async_smem();
+                mbar_arrive(&ctl->kv_full[(jj - 1) % kStages]);
+            }
+        }
+        cp_async_wait<0>();                // nothing in flight after this point
+        if (ok && issued > 0) {
+            fence_proxy_async_smem();
+            mbar_arrive(&ctl->kv_full[(issued - 1) % kStages]);
+        }
+        if (!ok) {
+            if (lane == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
+        }
+        __syncwarp();
+    } else if (warp == 0) {
         // ================= TMA producer =================
         const uint64_t policy = l2_policy_evict_last();
         bool ok = true;
@@ -291,7 +409,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         for (int jj = 0; jj < n && ok; ++jj) {
             const int st = jj % kStages;
             const int x = jj & 1;
-            const bool tail = (t0 + jj) * kBlockN + kBlockN > L;
+            const bool tail = !kSparse && (t0 + jj) * kBlockN + kBlockN > L;
             ok = tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
                       : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
             // S buffer x held tile jj - 2; the softmax threads have read it out
@@ -480,14 +598,30 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
             // the scale is positive, so the row max can be taken on raw scores and the scale
             // folded into the exponent's FMA below.
-            const int kpos = (t0 + jj) * kBlockN;
-            if (kpos + kBlockN > P) {
+            if constexpr (kSparse) {
+                int kind, base;
+                sparse_segment(t0 + jj, nA, nB, kind, base);
+                uint64_t vis;
+                if (kind == 2) {
+                    vis = base == 0 ? anc : 0ull;  // at most 64 tree tokens: one tree tile
+                } else {
+                    // the slot mask was written before the stage was released to QK
+                    const int st = jj % kStages;
+                    if (ok) ok = mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
+                    vis = kind == tok_local ? *reinterpret_cast<volatile uint64_t*>(&ctl->slot_mask[st]) : 0ull;
+                }
 #pragma unroll
-                for (int k = 0; k < kBlockN; ++k) {
-                    const int t = kpos + k;
-                    bool vis = t < P;
-                    if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
-                    s[k] = vis ? s[k] : -INFINITY;
+                for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;
+            } else {
+                const int kpos = (t0 + jj) * kBlockN;
+                if (kpos + kBlockN > P) {
+#pragma unroll
+                    for (int k = 0; k < kBlockN; ++k) {
+                        const int t = kpos + k;
+                        bool vis = t < P;
+                        if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
+                        s[k] = vis ? s[k] : -INFINITY;
+                    }
                 }
             }
             // tree reductions (8 independent chains) keep the dependent latency short

@@ -122,3 +122,26 @@ def test_kv_op_host_argument_checks(lib, op, over, code):
 def test_kv_op_specific_pointer_checks(lib):
     assert _kv_call("append", tree_kv=None) in (binding.MLA_ERR_INVALID_ARG, binding.MLA_ERR_NOT_INITIALIZED)
     assert binding.tree_kv_workspace_size() >= 4
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(topk=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(topk=binding.MAX_TOPK + 1), binding.MLA_ERR_UNSUPPORTED),
+    (dict(topk_idx=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), binding.MLA_ERR_INVALID_ARG),
+    (dict(num_heads=32), binding.MLA_ERR_UNSUPPORTED),
+])
+def test_sparse_host_argument_checks(lib, over, code):
+    args = dict(q_lat=16, q_rope=16, kv_cache=16, block_table=16, seq_lens=16, tree_parent=16, n_tree=16,
+                topk_idx=16, topk=512, scale=0.07, out=16, lse=16, stream=None, batch=1, total_q=1, max_tree=1,
+                max_seq_len=65, num_heads=64, page_size=64, num_pages=2, max_pages_per_seq=2, num_splits=0,
+                workspace=256, workspace_bytes=1 << 20)
+    args.update(over)
+    assert binding.verify_sparse_attn(**args) == code
+
+
+def test_sparse_split_choice_and_workspace(lib):
+    assert binding.sparse_num_splits(16, 512, 32, 512) >= 1
+    assert binding.sparse_num_splits(16, 512, 32, 512, requested=3) == 3
+    assert binding.sparse_workspace_size(16, 512, 32, 512) > 0
+    assert binding.lib().mla_verify_sparse_num_splits(1, 1, 1, 0, 64, 0) < 0

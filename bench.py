@@ -10,6 +10,7 @@ roofline target applies.  ``--workload`` selects another one.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3] [--splits S]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
   python bench.py --path append|accept   # the paged-cache steps around verify (GB/s)
+  python bench.py --path sparse [--topk 512]   # the sparse (top-k) verify variant
 
 For N > 1 (torchrun) every rank runs an independent replica of the workload
 on its own GPU (the path has no exchange step); value = all ranks' work over
@@ -42,8 +43,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["verify", "append", "accept"], default="verify",
-                    help="verify attention (default) or a paged-cache step around it")
+    ap.add_argument("--path", choices=["verify", "sparse", "append", "accept"], default="verify",
+                    help="verify attention (default), its sparse top-k variant, or a paged-cache step")
+    ap.add_argument("--topk", type=int, default=512, help="slots per tree token for --path sparse")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
     ap.add_argument("--splits", type=int, default=None, help="KV splits (0 = library's choice)")
     ap.add_argument("--seed", type=int, default=0)
@@ -182,14 +184,17 @@ def profiled_traffic(workload: str, launch_units: int):
     return int(entry["dram_bytes_per_launch"] * launch_units / entry.get("units", launch_units))
 
 
-def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7):
+def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7, topk_idx=None):
     import numpy as np
 
     import oracle
     from mla_speculative_decoding_verify_gb300 import inputs as I
     sample = I.sample_rows(inp, rows, seed=seed)
     t0 = time.perf_counter()
-    oracle.verify_rows(inp, sample)
+    if topk_idx is None:
+        oracle.verify_rows(inp, sample)
+    else:
+        oracle.verify_sparse_rows(inp, topk_idx, sample)
     dt = time.perf_counter() - t0
     total_rows = inp.total_q * inp.num_heads
     # flops of the sampled rows: rows share their request's key count
@@ -213,22 +218,39 @@ def run_ours(args, ranks: Ranks):
     binding.init(ranks.local)
     cfg = WORKLOADS[args.workload]
     inp = I.config_inputs(cfg, seed=args.seed)
-    flops = metrics.algorithmic_flops(inp)
-    kv_logical = metrics.kv_bytes(inp)
-    kv_unique = metrics.kv_bytes(inp, unique=True)
+    sparse = args.path == "sparse"
     io = metrics.io_bytes(inp)
+    if sparse:
+        topk_idx = I.topk_indices(inp, args.topk, seed=args.seed + 3)
+        flops = metrics.sparse_flops(inp, topk_idx)
+        kv_logical = kv_unique = metrics.sparse_kv_bytes(inp, topk_idx)
+        io["h2d"] += int(topk_idx.nbytes)
+        d_topk = torch.from_numpy(topk_idx).to(dev)
+    else:
+        flops = metrics.algorithmic_flops(inp)
+        kv_logical = metrics.kv_bytes(inp)
+        kv_unique = metrics.kv_bytes(inp, unique=True)
     db = binding.DeviceBatch(inp, dev)
-    splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
-                                args.splits)
+    if sparse:
+        splits = binding.sparse_num_splits(inp.batch, inp.total_q, inp.max_tree, args.topk, inp.num_heads,
+                                           args.splits)
+    else:
+        splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
+                                    args.splits)
     out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
-    ws = torch.empty(binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
-                                            inp.num_heads, splits), dtype=torch.uint8, device=dev)
+    ws_bytes = (binding.sparse_workspace_size(inp.batch, inp.total_q, inp.max_tree, args.topk, inp.num_heads, splits)
+                if sparse else binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
+                                                      inp.num_heads, splits))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
+        if sparse:
+            binding.verify_sparse(db, d_topk, splits, out=out, lse=lse, workspace=ws, stream=stream)
+        else:
+            binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -277,9 +299,14 @@ def run_ours(args, ranks: Ranks):
         h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
 
+        if sparse:
+            h_topk = torch.from_numpy(topk_idx).pin_memory()
+
         def e2e_step():
             for k, t in h.items():
                 getattr(db, k).copy_(t, non_blocking=True)
+            if sparse:
+                d_topk.copy_(h_topk, non_blocking=True)
             step()
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
@@ -309,9 +336,25 @@ def run_ours(args, ranks: Ranks):
     peak = float(peaks["bf16_tflops"])
     # units of one launch = (row tile, split) work units
     units = ((inp.n_tree + 1) // 2).sum() * splits
-    traffic = profiled_traffic(args.workload, int(units))
+    traffic = None if sparse else profiled_traffic(args.workload, int(units))
+    if sparse:
+        gbs = kv_logical / (t_kern * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                    "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                    "peak_source": f"{peak_kind} hbm_gbs, MEASURED_PEAKS.json" if peak_kind == "measured"
+                    else "fallback 6.8 TB/s",
+                    "kernel": "mla_verify_kernel<true>", "bytes_per_launch": kv_logical,
+                    "note": "algorithmic bytes = one 1152-byte KV row per visible key per tree token "
+                            "(121 flop/B, below the bf16 ridge)",
+                    "tflops": achieved}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": f"{peak_kind} bf16_tflops (burst), MEASURED_PEAKS.json"
+                    if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
+                    "kernel": "mla_verify_kernel", "flops_per_launch": flops}
     result = {
-        "metric": METRIC,
+        "metric": METRIC if not sparse else f"sparse verify-attn (top-k {args.topk}) TFLOP/s & gathered KV GB/s, 1 GB300",
         "value": whole_job_tflops(ranks.world, flops, t_step),
         "unit": "TFLOP/s",
         "n_gpus": ranks.world,
@@ -332,19 +375,17 @@ def run_ours(args, ranks: Ranks):
                     "hbm_peak": float(peaks["hbm_gbs"])},
         "algorithmic_gflop_per_step": flops / 1e9,
         "kernel_ms": t_kern,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16_tflops (burst), MEASURED_PEAKS.json"
-                     if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
-                     "kernel": "mla_verify_kernel", "flops_per_launch": flops},
+        "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clk,
         "device_status": status,
     }
     if e2e:
         result["e2e"] = e2e
+    if sparse:
+        result["config"]["topk"] = args.topk
     if ranks.rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(inp, flops, args.cpu_rows)
+        result["cpu_baseline"] = cpu_baseline(inp, flops, args.cpu_rows, topk_idx=topk_idx if sparse else None)
     return result
 
 
@@ -518,7 +559,7 @@ def main(argv=None):
         return 0
     ranks = Ranks("nccl")
     try:
-        res = run_ours(args, ranks) if args.path == "verify" else run_kv_op(args, ranks)
+        res = run_ours(args, ranks) if args.path in ("verify", "sparse") else run_kv_op(args, ranks)
         if ranks.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

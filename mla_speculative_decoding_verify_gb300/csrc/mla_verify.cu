@@ -317,7 +317,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
     if (g_prof_begin && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0)
-        mla::mla_verify_kernel<true><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+        mla::mla_verify_kernel<true><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     else
         mla::mla_verify_kernel<false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;

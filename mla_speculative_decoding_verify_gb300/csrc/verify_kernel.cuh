@@ -50,6 +50,8 @@ constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
 constexpr int kStages = 3;
 constexpr int kThreads = 224;          // warp 0 TMA, warp 1 QK MMAs, warps 2..5 softmax, warp 6 PV MMAs
+constexpr int kThreadsSparse = 256;    // sparse variant: warps 0 and 7 gather the KV rows
+constexpr int kGatherWarp2 = 7;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kPvWarp = 6;
 constexpr int kSoftmaxThreads = 128;
@@ -127,7 +129,7 @@ struct Ctrl {
     int abort;
     int lo_flag[2];
     int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
-    uint64_t slot_mask[kStages];  // sparse: bit k set if key k of the stage's tile is a real slot
+    uint32_t slot_mask[kStages][2];  // sparse: bit k of half h set if key 32h + k of the stage's tile is a real slot
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -155,7 +157,7 @@ __device__ __forceinline__ void sparse_segment(int j, int nA, int nB, int& kind,
 }
 
 template <bool kSparse>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
 mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap map_lat,
                   const __grid_constant__ CUtensorMap map_rope) {
     extern __shared__ uint8_t smem_raw[];
@@ -221,7 +223,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // ---- set-up ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->kv_full[s], kSparse ? 32 : 1);  // sparse: one arrival per producer lane
+            mbar_init(&ctl->kv_full[s], kSparse ? 64 : 1);  // sparse: one arrival per gathering lane
             mbar_init(&ctl->kv_empty[s], 1);
             mbar_init(&ctl->kv_fixed[s], 1);
         }
@@ -261,72 +263,70 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
     const uint32_t p_addr = smem_u32(smem + kOffP);
 
-    if (warp == 0 && kSparse) {
-        // ================= gather producer (sparse) =================
-        // Lane l fills keys l and l + 32 of each tile: this CTA's latent half
-        // (512 B as 4 x 8 16-byte units, 128B swizzle) and rope half (64 B, 64B
-        // swizzle).  Copies of tile jj are released to QK after tile jj + 1 was
+    if (kSparse && (warp == 0 || warp == kGatherWarp2)) {
+        // ================= gather producers (sparse) =================
+        // Lane l of gather warp h fills key 32h + l of each tile: this CTA's latent
+        // half (512 B as 4 x 8 16-byte units, 128B swizzle) and rope half (64 B,
+        // 64B swizzle).  The cache row of tile jj + 1 is looked up while tile jj's
+        // copies are in flight; tile jj is released to QK once tile jj + 1 has been
         // issued (cp.async groups, then a proxy fence and one arrival per lane).
+        const int key = (warp == 0 ? 0 : 32) + lane;
+        // cache row of this lane's key in local tile jj, or -1 for an empty slot
+        auto lookup = [&](int jj) -> long long {
+            int kind, base;
+            sparse_segment(t0 + jj, nA, nB, kind, base);
+            int pos = -1;
+            if (kind == 2) {
+                if (base + key < T) pos = P + base + key;
+            } else if (base + key < p.topk) {
+                pos = __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key);
+                if (pos >= P) pos = -1;   // rejected by the prep kernel; never read
+            }
+            if (pos < 0) return -1;
+            const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + pos / p.page_size);
+            if (page < 0 || page >= p.num_pages) {
+                raise_status(p.status, kStatusBadBlock);
+                return -1;
+            }
+            return static_cast<long long>(page) * p.page_size + pos % p.page_size;
+        };
         bool ok = true;
         int issued = 0;
+        long long row = n > 0 ? lookup(0) : -1;
         for (int jj = 0; jj < n && ok; ++jj) {
             const int st = jj % kStages;
             if (jj >= kStages) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
                 if (!ok) break;
             }
-            int kind, base;
-            sparse_segment(t0 + jj, nA, nB, kind, base);
             const uint32_t sb = stage0 + st * kStageBytes;
-            bool valid[2];
+            const uint32_t lat = sb + key * 128;
+            const uint32_t rope = sb + 4 * kChunkBytes + key * 64;
+            const bool valid = row >= 0;
+            if (valid) {
+                const uint8_t* src = p.kv_bytes + row * (kDqk * 2);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int key = lane + 32 * h;
-                int pos = -1;
-                if (kind == 2) {
-                    if (base + key < T) pos = P + base + key;
-                } else if (base + key < p.topk) {
-                    pos = __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key);
-                    if (pos >= P) pos = -1;   // rejected by the prep kernel; never read
-                }
-                long long row = -1;
-                if (pos >= 0) {
-                    const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + pos / p.page_size);
-                    if (page >= 0 && page < p.num_pages) {
-                        row = static_cast<long long>(page) * p.page_size + pos % p.page_size;
-                    } else {
-                        raise_status(p.status, kStatusBadBlock);
-                    }
-                }
-                valid[h] = row >= 0;
-                const uint32_t lat = sb + key * 128;
-                const uint32_t rope = sb + 4 * kChunkBytes + key * 64;
-                if (valid[h]) {
-                    const uint8_t* src = p.kv_bytes + row * (kDqk * 2);
+                for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
+                    for (int u = 0; u < 8; ++u)
+                        cp_async_16(lat + ch * kChunkBytes + ((u ^ (key & 7)) << 4),
+                                    src + kDLatentHalf * 2 * c + 128 * ch + 16 * u);
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            cp_async_16(lat + ch * kChunkBytes + ((u ^ (key & 7)) << 4),
-                                        src + kDLatentHalf * 2 * c + 128 * ch + 16 * u);
+                for (int u = 0; u < 4; ++u)
+                    cp_async_16(rope + ((u ^ ((key >> 1) & 3)) << 4), src + kDLatent * 2 + kDRopeHalf * 2 * c + 16 * u);
+            } else {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        cp_async_16(rope + ((u ^ ((key >> 1) & 3)) << 4), src + kDLatent * 2 + kDRopeHalf * 2 * c + 16 * u);
-                } else {
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
+                    for (int u = 0; u < 8; ++u) st_shared_v4(lat + ch * kChunkBytes + (u << 4), 0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) st_shared_v4(lat + ch * kChunkBytes + (u << 4), z.x, z.y, z.z, z.w);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) st_shared_v4(rope + (u << 4), z.x, z.y, z.z, z.w);
-                }
+                for (int u = 0; u < 4; ++u) st_shared_v4(rope + (u << 4), 0.f, 0.f, 0.f, 0.f);
             }
-            const uint32_t lo_bits = __ballot_sync(0xffffffffu, valid[0]);
-            const uint32_t hi_bits = __ballot_sync(0xffffffffu, valid[1]);
-            if (lane == 0) ctl->slot_mask[st] = (static_cast<uint64_t>(hi_bits) << 32) | lo_bits;
+            const uint32_t bits = __ballot_sync(0xffffffffu, valid);
+            if (lane == 0) ctl->slot_mask[st][key >> 5] = bits;
             cp_async_commit();
             ++issued;
+            if (jj + 1 < n) row = lookup(jj + 1);   // in flight with this tile's copies
             if (jj >= 1) {
                 cp_async_wait<1>();        // tile jj - 1 has landed
                 fence_proxy_async_smem();
@@ -608,7 +608,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     // the slot mask was written before the stage was released to QK
                     const int st = jj % kStages;
                     if (ok) ok = mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
-                    vis = kind == tok_local ? *reinterpret_cast<volatile uint64_t*>(&ctl->slot_mask[st]) : 0ull;
+                    const volatile uint32_t* sm = ctl->slot_mask[st];
+                    vis = kind == tok_local ? (static_cast<uint64_t>(sm[1]) << 32) | sm[0] : 0ull;
                 }
 #pragma unroll
                 for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;

@@ -35,6 +35,27 @@ def algorithmic_flops(inp) -> int:
     return int(total)
 
 
+def sparse_visible_keys(inp, topk_idx: np.ndarray) -> int:
+    """Sum over tree tokens of their visible keys in the sparse variant: listed
+    slots plus ancestor-or-self tree tokens."""
+    total = int((np.asarray(topk_idx) >= 0).sum())
+    off = 0
+    for b in range(inp.batch):
+        T = int(inp.n_tree[b])
+        total += visible_tree_pairs(inp.tree_parent[off:off + T])
+        off += T
+    return total
+
+
+def sparse_flops(inp, topk_idx: np.ndarray) -> int:
+    return int(inp.num_heads * FLOPS_PER_ROW_KEY * sparse_visible_keys(inp, topk_idx))
+
+
+def sparse_kv_bytes(inp, topk_idx: np.ndarray) -> int:
+    """KV rows the sparse variant must read: each visible key once per tree token."""
+    return int(sparse_visible_keys(inp, topk_idx) * KV_ROW_BYTES)
+
+
 def kv_bytes(inp, unique: bool = False) -> int:
     if not unique:
         return int(inp.seq_lens.astype(np.int64).sum()) * KV_ROW_BYTES

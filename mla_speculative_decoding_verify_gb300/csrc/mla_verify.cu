@@ -41,11 +41,11 @@ int current_device() {
 
 // Workspace layout shared by the size query and the launch.
 struct Layout {
-    size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, total;
+    size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, tok_req, total;
     int max_items;
 };
 
-Layout make_layout(int batch, int total_q, int num_splits) {
+Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false) {
     Layout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -69,6 +69,7 @@ Layout make_layout(int batch, int total_q, int num_splits) {
     } else {
         L.part_out = L.part_lse = 0;
     }
+    L.tok_req = sparse ? take(sizeof(int32_t) * (total_q > 0 ? total_q : 1)) : 0;
     L.total = off;
     return L;
 }
@@ -242,7 +243,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     const int splits = topk > 0 ? mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits)
                                 : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (splits <= 0) return MLA_ERR_INVALID_ARG;
-    const Layout lay = make_layout(batch, total_q, splits);
+    const Layout lay = make_layout(batch, total_q, splits, topk > 0);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_WORKSPACE;
 
@@ -280,10 +281,18 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_pages = max_pages_per_seq;
     pp.num_pages = num_pages;
     pp.max_items = lay.max_items;
-    pp.topk_idx = topk_idx;
-    pp.topk = topk;
+    pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (topk > 0) {
+        const long long entries = static_cast<long long>(total_q) * topk;
+        const long long want = (entries + 4LL * mla::kCheckThreads - 1) / (4LL * mla::kCheckThreads);
+        const unsigned blocks =
+            static_cast<unsigned>(std::max(1LL, std::min<long long>(want, 4LL * sm_count_of_current())));
+        mla::mla_topk_check_kernel<<<blocks, mla::kCheckThreads, 0, stream>>>(
+            topk_idx, topk, entries, pp.tok_req, seq_lens, n_tree, batch, req_state, status);
+        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    }
 
     // ---- fused verify attention ----
     mla::VerifyParams vp{};
@@ -351,7 +360,7 @@ size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, in
                                         int num_splits) {
     const int s = mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits);
     if (s <= 0) return 0;
-    return make_layout(batch, total_q, s).total;
+    return make_layout(batch, total_q, s, true).total;
 }
 
 int mla_verify_sparse_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,

@@ -31,8 +31,7 @@ struct PrepParams {
     int32_t* item_count;         // [1]
     int* status;                 // [1]
     int batch, total_q, page_size, max_pages, num_pages, max_items;
-    const int32_t* topk_idx;     // sparse variant: [total_q, topk], else null
-    int topk;
+    int32_t* tok_req;            // sparse variant: [total_q] request of each tree token (-1 if malformed), else null
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
@@ -82,6 +81,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     }
     __syncthreads();
 
+    // 0. sparse variant: no token belongs to a request until step 2 says so
+    if (p.tok_req)
+        for (int g = tid; g < p.total_q; g += kPrepThreads) p.tok_req[g] = -1;
+
     // 1. query offsets (exclusive scan of n_tree)
     block_exclusive_scan(p.batch, [&](int b) { return p.n_tree[b]; }, p.q_off, warp_sums);
     if (tid == 0 && p.q_off[p.batch] != p.total_q) atomicOr(p.status, kStatusBadTree);
@@ -112,24 +115,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
                 }
             }
         }
-        // sparse variant: every slot is -1 or a prefix position
-        bool bad_index = false;
-        if (shape_ok && p.topk > 0) {
-            const long long n = static_cast<long long>(T) * p.topk;
-            const int32_t* idx = p.topk_idx + static_cast<long long>(base) * p.topk;
-            for (long long k = lane; k < n; k += 32) {
-                const int v = __ldg(idx + k);
-                bad_index |= v < -1 || v >= L - T;
-            }
-        }
+        if (shape_ok && p.tok_req)
+            for (int i = lane; i < T; i += 32) p.tok_req[base + i] = b;
         bad_parent = __any_sync(0xffffffffu, bad_parent);
         bad_block = __any_sync(0xffffffffu, bad_block);
-        bad_index = __any_sync(0xffffffffu, bad_index);
-        const bool all_ok = shape_ok && !bad_parent && !bad_block && !bad_index;
+        const bool all_ok = shape_ok && !bad_parent && !bad_block;
         if (lane == 0) {
             p.req_state[b] = shape_ok ? (all_ok ? 0 : 1) : 2;  // 2: outputs not written at all
-            const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0) |
-                             (bad_index ? kStatusBadIndex : 0);
+            const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0);
             if (bits) atomicOr(p.status, bits);
         }
         __syncwarp();
@@ -207,6 +200,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     if (tid == 0) {
         *p.item_count = total_items;
         if (p.item_off[p.batch] > p.max_items) atomicOr(p.status, kStatusBadTree);
+    }
+}
+
+// Sparse variant: every top-k slot must be -1 or a prefix position of its
+// token's request; otherwise the request's rows are written as out = 0,
+// lse = -inf and the status gets kStatusBadIndex.  Grid-stride, coalesced.
+constexpr int kCheckThreads = 256;
+
+__global__ void __launch_bounds__(kCheckThreads) mla_topk_check_kernel(const int32_t* topk_idx, int topk,
+                                                                     long long entries, const int32_t* tok_req,
+                                                                     const int32_t* seq_lens, const int32_t* n_tree,
+                                                                     int batch, int32_t* req_state, int* status) {
+    for (long long e = blockIdx.x * static_cast<long long>(kCheckThreads) + threadIdx.x; e < entries;
+         e += static_cast<long long>(gridDim.x) * kCheckThreads) {
+        const int v = __ldg(topk_idx + e);
+        const int b = __ldg(tok_req + e / topk);
+        if (b < 0 || b >= batch) continue;   // token of a malformed request
+        const int P = __ldg(seq_lens + b) - __ldg(n_tree + b);
+        if (v < -1 || v >= P) {
+            if (req_state[b] == 0) req_state[b] = 1;
+            atomicOr(status, kStatusBadIndex);
+        }
     }
 }
 

@@ -125,12 +125,15 @@ int sparse_tiles(int topk) { return 2 * ((topk + mla::kBlockN - 1) / mla::kBlock
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int encode_maps(const void* kv_cache, long long rows, CUtensorMap* lat, CUtensorMap* rope) {
+// Maps over the cache as a [rows, 576] bf16 tensor: 64-dim latent chunks (128B
+// swizzle) and 32-dim rope halves (64B swizzle).  box_rows is 64 for a dense
+// tile and 1 for the sparse variant's four-row gathers.
+int encode_maps(const void* kv_cache, long long rows, unsigned box_rows, CUtensorMap* lat, CUtensorMap* rope) {
     if (!g_encode) return MLA_ERR_NOT_INITIALIZED;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLA_D_LATENT + MLA_D_ROPE), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>((MLA_D_LATENT + MLA_D_ROPE) * 2)};
-    const cuuint32_t box_lat[2] = {64, static_cast<cuuint32_t>(mla::kBlockN)};
-    const cuuint32_t box_rope[2] = {static_cast<cuuint32_t>(mla::kDRopeHalf), static_cast<cuuint32_t>(mla::kBlockN)};
+    const cuuint32_t box_lat[2] = {64, box_rows};
+    const cuuint32_t box_rope[2] = {static_cast<cuuint32_t>(mla::kDRopeHalf), box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r1 = g_encode(lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims, strides,
                            box_lat, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -258,7 +261,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     float* part_lse = splits > 1 ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
 
     CUtensorMap map_lat, map_rope;
-    const int enc = encode_maps(kv_cache, static_cast<long long>(num_pages) * page_size, &map_lat, &map_rope);
+    const int enc = encode_maps(kv_cache, static_cast<long long>(num_pages) * page_size,
+                                topk > 0 ? 1u : static_cast<unsigned>(mla::kBlockN), &map_lat, &map_rope);
     if (enc != MLA_OK) return enc;
 
     // ---- prep: offsets, ancestor bit sets, validation, work list ----
@@ -321,8 +325,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.scale_log2 = scale * 1.4426950408889634f;
     vp.timeout_ns = kDefaultTimeoutNs;
     vp.topk_idx = topk_idx;
-    vp.kv_bytes = static_cast<const uint8_t*>(kv_cache);
     vp.topk = topk;
+    vp.kv = static_cast<const uint16_t*>(kv_cache);
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
     if (g_prof_begin && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0)

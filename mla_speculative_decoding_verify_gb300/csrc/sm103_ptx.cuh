@@ -177,17 +177,9 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
     return out != 0;
 }
 
-// ------------------------------------------------------------------ per-thread async copies
-
-// 16-byte global -> shared copy (L2 only); completes asynchronously.
-__device__ __forceinline__ void cp_async_16(uint32_t smem_addr, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most N of this thread's committed groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Bring the 128-byte line holding `gmem` into L2 (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* gmem) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem));
 }
 
 // ------------------------------------------------------------------ TMA
@@ -204,6 +196,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// Four-row gather: rows y0..y3 of a 2-D tensor, columns [x, x + box width),
+// into four consecutive box rows at dst (the map's box is one row high).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "l"(policy)
         : "memory");
 }
 

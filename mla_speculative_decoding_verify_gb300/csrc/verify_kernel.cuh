@@ -26,9 +26,9 @@
 // tokens): tree token g sees the prefix positions listed in its topk slots and
 // its ancestor-or-self tree tokens.  A row tile's key sequence is token 0's
 // slots, then token 1's slots, then the tree keys; rows see only their own
-// token's slots.  Warp 0 gathers the rows with per-thread 16-byte async
-// copies into the same swizzled stage layout (empty slots are zero-filled) and
-// records which of the tile's 64 slots are real.
+// token's slots.  Two TMA warps gather the rows with four-row tensor gathers
+// into the same swizzled stage layout (empty slots read as zeros) and records
+// which of the tile's 64 slots are real.
 // TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
 #pragma once
 
@@ -107,7 +107,7 @@ struct VerifyParams {
     uint64_t timeout_ns;
     // sparse variant only
     const int32_t* topk_idx;    // [total_q, topk] prefix positions, -1 = unused slot
-    const uint8_t* kv_bytes;    // the cache as bytes, rows of 1152
+    const uint16_t* kv;         // the cache [num_pages * page_size, 576] (L2 prefetch of gathered rows)
     int topk;
 };
 
@@ -220,10 +220,32 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         return;
     }
 
+    // Sparse gather warps: lane l of warp h handles key 32h + l of every tile.
+    // The slot values of the first tiles are loaded before the set-up below.
+    [[maybe_unused]] const int half = warp == 0 ? 0 : 1;
+    [[maybe_unused]] const int key = 32 * half + lane;
+    // raw slot value of this lane's key in local tile jj (a KV position, -1 for none)
+    [[maybe_unused]] auto slot_raw = [&](int jj) -> int {
+        if (jj >= n) return -1;
+        int kind, base;
+        sparse_segment(t0 + jj, nA, nB, kind, base);
+        if (kind == 2) return base + key < T ? P + base + key : -1;
+        return base + key < p.topk
+                   ? __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key)
+                   : -1;
+    };
+    [[maybe_unused]] int pre_raw[3] = {-1, -1, -1};
+    if constexpr (kSparse) {
+        if (warp == 0 || warp == kGatherWarp2) {
+#pragma unroll
+            for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(t);
+        }
+    }
+
     // ---- set-up ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->kv_full[s], kSparse ? 64 : 1);  // sparse: one arrival per gathering lane
+            mbar_init(&ctl->kv_full[s], kSparse ? 2 : 1);  // sparse: one arrival per gather warp
             mbar_init(&ctl->kv_empty[s], 1);
             mbar_init(&ctl->kv_fixed[s], 1);
         }
@@ -263,131 +285,142 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
     const uint32_t p_addr = smem_u32(smem + kOffP);
 
-    if (kSparse && (warp == 0 || warp == kGatherWarp2)) {
-        // ================= gather producers (sparse) =================
-        // Lane l of gather warp h fills key 32h + l of each tile: this CTA's latent
-        // half (512 B as 4 x 8 16-byte units, 128B swizzle) and rope half (64 B,
-        // 64B swizzle).  The cache row of tile jj + 1 is looked up while tile jj's
-        // copies are in flight; tile jj is released to QK once tile jj + 1 has been
-        // issued (cp.async groups, then a proxy fence and one arrival per lane).
-        const int key = (warp == 0 ? 0 : 32) + lane;
-        // cache row of this lane's key in local tile jj, or -1 for an empty slot
-        auto lookup = [&](int jj) -> long long {
+    if (warp == 0 || (kSparse && warp == kGatherWarp2)) {
+        // ================= TMA producer(s) =================
+        // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: warps 0
+        // and kGatherWarp2 each own 32 keys of every tile (TMA instructions issued
+        // by the lanes of one warp are serialised, so two warps halve the issue
+        // time).  Lane l looks up the cache row of key 32h + l; lanes 0..7 then
+        // load keys 32h + 4l .. 32h + 4l + 3 with four-row gathers (one box row
+        // per key), and each warp posts its half of the tile's bytes on the stage
+        // barrier, so a gathered tile completes exactly like a dense one.  Empty
+        // slots name a row past the end of the cache and read as zeros.  The
+        // lookups run ahead of the copies: before tile jj waits for its stage,
+        // the row of tile jj + 1 is completed and prefetched into L2, and the
+        // block-table entry of tile jj + 2 and the slot value of tile jj + 3 are
+        // loaded; each loaded value is first used one tile later.
+        const uint64_t policy = l2_policy_evict_last();
+        bool ok = true;
+        int issued = 0;
+        // checked position of a raw slot value of tile jt (slot positions the check
+        // kernel rejected, >= P, are dropped); its block-table load is issued, not waited on
+        [[maybe_unused]] auto translate = [&](int jt, int raw, int& tpos, int& page) {
             int kind, base;
-            sparse_segment(t0 + jj, nA, nB, kind, base);
-            int pos = -1;
-            if (kind == 2) {
-                if (base + key < T) pos = P + base + key;
-            } else if (base + key < p.topk) {
-                pos = __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key);
-                if (pos >= P) pos = -1;   // rejected by the prep kernel; never read
-            }
-            if (pos < 0) return -1;
-            const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + pos / p.page_size);
+            sparse_segment(t0 + jt, nA, nB, kind, base);
+            tpos = (raw < 0 || (kind != 2 && raw >= P)) ? -1 : raw;
+            page = tpos >= 0 ? __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + tpos / p.page_size)
+                             : -1;
+        };
+        // cache row from a checked position and its (landed) block-table entry
+        [[maybe_unused]] auto row_of = [&](int tpos, int page) -> int {
+            if (tpos < 0) return -1;
             if (page < 0 || page >= p.num_pages) {
                 raise_status(p.status, kStatusBadBlock);
                 return -1;
             }
-            return static_cast<long long>(page) * p.page_size + pos % p.page_size;
+            return page * p.page_size + tpos % p.page_size;
         };
-        bool ok = true;
-        int issued = 0;
-        long long row = n > 0 ? lookup(0) : -1;
+        // this CTA's 576 bytes of a row span five 128-byte lines
+        [[maybe_unused]] auto prefetch_row = [&](int row) {
+            if (row < 0) return;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.kv) + static_cast<long long>(row) * (kDqk * 2);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) prefetch_l2(src + kDLatentHalf * 2 * c + 128 * ch);
+            prefetch_l2(src + kDLatent * 2 + kDRopeHalf * 2 * c);
+        };
+        [[maybe_unused]] int raw = -1;   // slot value (tile jj + 3)
+        [[maybe_unused]] int tpos = -1;  // checked position (tile jj + 2) ...
+        [[maybe_unused]] int page = -1;  // ... and its block-table entry, in flight
+        [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
+        [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
+        [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
+        if constexpr (kSparse) {
+            // slot values of tiles 0..2 were loaded before the set-up; the
+            // block-table entries of tiles 0 and 1 are one more round trip
+            raw = pre_raw[2];
+            int tpos0, page0;
+            translate(0, pre_raw[0], tpos0, page0);
+            translate(1, pre_raw[1], tpos, page);
+            cur = row_of(tpos0, page0);
+            prefetch_row(cur);
+        }
         for (int jj = 0; jj < n && ok; ++jj) {
             const int st = jj % kStages;
-            if (jj >= kStages) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
-                if (!ok) break;
-            }
-            const uint32_t sb = stage0 + st * kStageBytes;
-            const uint32_t lat = sb + key * 128;
-            const uint32_t rope = sb + 4 * kChunkBytes + key * 64;
-            const bool valid = row >= 0;
-            if (valid) {
-                const uint8_t* src = p.kv_bytes + row * (kDqk * 2);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        cp_async_16(lat + ch * kChunkBytes + ((u ^ (key & 7)) << 4),
-                                    src + kDLatentHalf * 2 * c + 128 * ch + 16 * u);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    cp_async_16(rope + ((u ^ ((key >> 1) & 3)) << 4), src + kDLatent * 2 + kDRopeHalf * 2 * c + 16 * u);
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) st_shared_v4(lat + ch * kChunkBytes + (u << 4), 0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) st_shared_v4(rope + (u << 4), 0.f, 0.f, 0.f, 0.f);
-            }
-            const uint32_t bits = __ballot_sync(0xffffffffu, valid);
-            if (lane == 0) ctl->slot_mask[st][key >> 5] = bits;
-            cp_async_commit();
-            ++issued;
-            if (jj + 1 < n) row = lookup(jj + 1);   // in flight with this tile's copies
-            if (jj >= 1) {
-                cp_async_wait<1>();        // tile jj - 1 has landed
-                fence_proxy_async_smem();
-                mbar_arrive(&ctl->kv_full[(jj - 1) % kStages]);
-            }
-        }
-        cp_async_wait<0>();                // nothing in flight after this point
-        if (ok && issued > 0) {
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl->kv_full[(issued - 1) % kStages]);
-        }
-        if (!ok) {
-            if (lane == 0) raise_status(p.status, kStatusTimeout);
-            *abort_flag = 1;
-        }
-        __syncwarp();
-    } else if (warp == 0) {
-        // ================= TMA producer =================
-        const uint64_t policy = l2_policy_evict_last();
-        bool ok = true;
-        int issued = 0;
-        for (int jj = 0; jj < n && ok; ++jj) {
-            const int st = jj % kStages;
-            if (jj >= kStages) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
-                if (!ok) break;
-            }
-            const int kpos = (t0 + jj) * kBlockN;
-            if (lane == 0) {
-                const int page_idx = kpos / p.page_size;
-                const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + page_idx);
-                if (page < 0 || page >= p.num_pages) raise_status(p.status, kStatusBadBlock);
-                // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
-                const int row = page * p.page_size + (kpos % p.page_size);
-                uint8_t* dst = smem + kOffStages + st * kStageBytes;
-                mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
-                for (int ch = 0; ch < 4; ++ch)
-                    tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
-                                kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
-                tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
-                            kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
-            }
-            ++issued;
-            __syncwarp();
-            if (kpos + kBlockN > L) {
-                // Last, partial tile: zero the rows past seq_len so that masked
-                // keys multiply finite values in PV.
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim));
-                if (!ok) break;
-                const int kvalid = L - kpos;
-                uint8_t* base = smem + kOffStages + st * kStageBytes;
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
-                    const int u = lane % 8;  // 16-byte unit of the row
-                    for (int ch = 0; ch < 4; ++ch)
-                        *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
-                    if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+            if constexpr (kSparse) {
+                if (jj + 1 < n) {
+                    nxt = row_of(tpos, page);
+                    prefetch_row(nxt);
                 }
-                fence_proxy_async_smem();
+                if (jj + 2 < n) {
+                    translate(jj + 2, raw, tpos, page);
+                    raw = slot_raw(jj + 3);
+                }
+            }
+            if (jj >= kStages) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
+                if (!ok) break;
+            }
+            uint8_t* dst = smem + kOffStages + st * kStageBytes;
+            if constexpr (kSparse) {
+                const uint32_t mask = __ballot_sync(0xffffffffu, cur >= 0);
+                int y[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int v = __shfl_sync(0xffffffffu, cur, (4 * lane + t) & 31);
+                    y[t] = v >= 0 ? v : oob_row;
+                }
+                if (lane == 0) {
+                    ctl->slot_mask[st][half] = mask;
+                    mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes / 2);  // releases the mask with the tile
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                if (lane < 8) {
+                    const int g = 8 * half + lane;  // keys 4g .. 4g + 3
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
+                                    kDLatentHalf * static_cast<int>(c) + 64 * ch, y[0], y[1], y[2], y[3], policy);
+                    tma_gather4(dst + 4 * kChunkBytes + 4 * g * 64, &map_rope, &ctl->kv_full[st],
+                                kDLatent + kDRopeHalf * static_cast<int>(c), y[0], y[1], y[2], y[3], policy);
+                }
+                cur = nxt;
+                ++issued;
+                __syncwarp();
+            } else {
+                const int kpos = (t0 + jj) * kBlockN;
+                if (lane == 0) {
+                    const int page_idx = kpos / p.page_size;
+                    const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + page_idx);
+                    if (page < 0 || page >= p.num_pages) raise_status(p.status, kStatusBadBlock);
+                    // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
+                    const int row = page * p.page_size + (kpos % p.page_size);
+                    mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
+                    for (int ch = 0; ch < 4; ++ch)
+                        tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
+                                    kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
+                    tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
+                                kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
+                }
+                ++issued;
+                __syncwarp();
+                if (kpos + kBlockN > L) {
+                    // Last, partial tile: zero the rows past seq_len so that masked
+                    // keys multiply finite values in PV.
+                    ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim));
+                    if (!ok) break;
+                    const int kvalid = L - kpos;
+                    uint8_t* base = smem + kOffStages + st * kStageBytes;
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
+                        const int u = lane % 8;  // 16-byte unit of the row
+                        for (int ch = 0; ch < 4; ++ch)
+                            *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
+                        if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                }
             }
         }
         if (!ok) {

@@ -336,11 +336,11 @@ def run_ours(args, ranks: Ranks):
     peak = float(peaks["bf16_tflops"])
     # units of one launch = (row tile, split) work units
     units = ((inp.n_tree + 1) // 2).sum() * splits
-    traffic = None if sparse else profiled_traffic(args.workload, int(units))
+    traffic = profiled_traffic(f"{args.workload}/sparse-top{args.topk}" if sparse else args.workload, int(units))
     if sparse:
         gbs = kv_logical / (t_kern * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                    "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                    "frac": gbs / float(peaks["hbm_gbs"]), "traffic": traffic,
                     "peak_source": f"{peak_kind} hbm_gbs, MEASURED_PEAKS.json" if peak_kind == "measured"
                     else "fallback 6.8 TB/s",
                     "kernel": "mla_verify_kernel<true>", "bytes_per_launch": kv_logical,

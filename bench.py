@@ -31,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "verify-attn TFLOP/s & KV GB/s, % of roofline, 1 GB300, prefix 4k-64k"
-WORKLOADS = {"c2": 2, "c3": 3, "c4": 4, "c5": 5}
+WORKLOADS = {"c1": 1, "c2": 2, "c3": 3, "c4": 4, "c5": 5}
 DEFAULT_SPLITS = {"c4": 16}
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -43,7 +43,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["verify", "sparse", "append", "accept"], default="verify",
+    ap.add_argument("--path", choices=["verify", "sparse", "append", "accept", "graph"], default="verify",
                     help="verify attention (default), its sparse top-k variant, or a paged-cache step")
     ap.add_argument("--topk", type=int, default=512, help="slots per tree token for --path sparse")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
@@ -509,6 +509,141 @@ def run_kv_op(args, ranks: Ranks):
     return result
 
 
+# ------------------------------------------------------------------ graph replay leg
+
+def run_graph(args, ranks: Ranks):
+    """Small-batch step latency: the whole verify step (prep, verify, combine)
+    replayed from a CUDA graph captured for the workload's bucket, against the
+    same step launched eagerly.  Latency = host launch to stream completion."""
+    import numpy as np
+    import torch
+
+    from mla_speculative_decoding_verify_gb300 import binding, inputs as I, metrics
+
+    dev = torch.device(f"cuda:{ranks.local}")
+    torch.cuda.set_device(dev)
+    binding.init(ranks.local)
+    inp = I.config_inputs(WORKLOADS[args.workload], seed=args.seed)
+    flops = metrics.algorithmic_flops(inp)
+    db = binding.DeviceBatch(inp, dev)
+    splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
+                                args.splits or 0)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
+                                            splits), dtype=torch.uint8, device=dev)
+    g = binding.VerifyGraph(db.kv_cache, inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.page_size,
+                            inp.max_pages_per_seq, inp.scale, num_splits_req=splits, stream=stream)
+    g.load(inp)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def eager():
+        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
+
+    def replay():
+        g.launch()
+
+    for _ in range(args.warmup):
+        eager()
+        replay()
+    torch.cuda.synchronize(dev)
+    status = binding.read_status(ws.data_ptr()) | binding.read_status(g.workspace.data_ptr())
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+    if not torch.equal(out, g.out[:inp.total_q]) or not torch.equal(lse, g.lse[:inp.total_q]):
+        raise RuntimeError("graph replay and eager step differ")
+
+    K = args.steps
+
+    def host_latency(fn):
+        t = []
+        for _ in range(K):
+            flush.zero_()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            stream.synchronize()
+            t.append(time.perf_counter() - t0)
+        return float(np.median(t)) * 1e6
+
+    def device_time(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
+
+    clocks = ClockSampler(ranks.local)
+    clocks.start()
+    time.sleep(0.3)
+    ranks.barrier()
+    torch.cuda.synchronize(dev)
+    lat_graph = host_latency(replay)
+    lat_eager = host_latency(eager)
+    dev_graph = device_time(replay)
+    dev_eager = device_time(eager)
+    ranks.barrier()
+    clk = clocks.stop()
+    lat_graph = ranks.max(lat_graph, dev)
+
+    # end to end: the step's query and tree inputs from pinned host memory into the
+    # graph's buffers, the replay, and out / lse back (the KV cache stays resident)
+    def pin(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(dt)).pin_memory()
+    h_in = [(g.q_lat[:inp.total_q], pin(inp.q_lat, np.int16)), (g.q_rope[:inp.total_q], pin(inp.q_rope, np.int16)),
+            (g.block_table[:inp.batch], pin(inp.block_table, np.int32)), (g.seq_lens, pin(inp.seq_lens, np.int32)),
+            (g.n_tree, pin(inp.n_tree, np.int32)), (g.tree_parent[:inp.total_q], pin(inp.tree_parent, np.int32))]
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for d, h in h_in:
+            d.copy_(h.view(d.shape), non_blocking=True)
+        g.launch()
+        h_out.copy_(g.out[:inp.total_q], non_blocking=True)
+        h_lse.copy_(g.lse[:inp.total_q], non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    lat_e2e = ranks.max(host_latency(e2e_step), dev)
+    h2d = sum(h.numel() * h.element_size() for _, h in h_in)
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    peaks, peak_kind = measured_peaks()
+    achieved = flops / (dev_graph * 1e-6) / 1e12
+    result = {
+        "metric": "verify step latency, CUDA-graph replay at the batch bucket (host launch to completion), 1 GB300",
+        "value": lat_graph, "unit": "us", "n_gpus": ranks.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": lat_graph * 1e-3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": inp.name, "batch": inp.batch, "tree_tokens": inp.total_q,
+                   "max_seq_len": inp.max_seq_len, "num_splits": splits, "bucket": [inp.batch, inp.total_q],
+                   "seed": args.seed, "parallelism": f"replicas x{ranks.world}",
+                   "l2": "flushed before every timed step (256 MiB write, not timed)"},
+        "eager_us": lat_eager, "graph_device_us": dev_graph, "eager_device_us": dev_eager,
+        "speedup_vs_eager": lat_eager / lat_graph,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                     "frac": achieved / float(peaks["bf16_tflops"]), "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops, MEASURED_PEAKS.json" if peak_kind == "measured"
+                     else "fallback 1.9 PFLOP/s bf16",
+                     "kernel": "whole replayed step", "flops_per_launch": flops,
+                     "note": "small batches are launch- and latency-bound; the fraction is context only"},
+        "e2e": {"value": lat_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": lat_e2e * 1e-3},
+        "gpu_launches": (3 if splits > 1 else 2) * K * 5,   # graph and eager: latency and event loops; e2e
+        "clocks": clk,
+        "device_status": status,
+    }
+    if ranks.rank == 0 and not args.no_cpu_baseline:
+        rows = min(args.cpu_rows, inp.total_q * inp.num_heads)
+        result["cpu_baseline"] = cpu_baseline(inp, flops, rows)
+    g.close()
+    return result
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, ranks: Ranks):
@@ -559,7 +694,12 @@ def main(argv=None):
         return 0
     ranks = Ranks("nccl")
     try:
-        res = run_ours(args, ranks) if args.path in ("verify", "sparse") else run_kv_op(args, ranks)
+        if args.path in ("verify", "sparse"):
+            res = run_ours(args, ranks)
+        elif args.path == "graph":
+            res = run_graph(args, ranks)
+        else:
+            res = run_kv_op(args, ranks)
         if ranks.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -261,6 +261,46 @@ int mla_tree_kv_accept(void *kv_cache, const int32_t *block_table, const int32_t
                        void *workspace, size_t workspace_bytes);
 
 /*
+ * Replayable verify step for a batch bucket (a CUDA graph of prep, slot check,
+ * verify and combine, captured once).  Serving loops run the same step shape
+ * every iteration at small batch, where launch overhead dominates.  A graph
+ * replays its GPU work with no host involvement, so everything that
+ * synchronises or chooses a configuration happens before the capture and the
+ * captured shape is a batch bucket that smaller batches pad up to (page "SMEM
+ * Ceiling", section "CUDA Graph Capture Safety: A Nuanced Understanding").
+ *
+ * mla_verify_graph_create: captures the step on `stream` (a private stream if
+ * it is a default stream) for the bucket max_batch requests, max_total_q tree
+ * tokens, with the arguments of mla_verify_attn (topk == 0) or
+ * mla_verify_sparse_attn (topk > 0).  The buffers passed here are the ones
+ * every replay reads and writes: the caller owns them, keeps them alive until
+ * mla_verify_graph_destroy, and writes each step's inputs into them before a
+ * launch.  Requires mla_init on the current device.  On success *graph holds
+ * a host object; on error *graph is NULL and nothing was launched.
+ *
+ * mla_verify_graph_launch: replays the step for the first `batch` requests
+ * (0 <= batch <= max_batch) on `stream`.  Requests batch .. max_batch - 1 are
+ * padded: their n_tree and seq_lens entries are set to 0 on the stream
+ * before the replay (so those entries of the caller's buffers are written).
+ * The tree tokens of the real requests must number at most max_total_q; out
+ * and lse rows past their total are not defined.  Errors are reported in the
+ * workspace's status word as for mla_verify_attn.  Call it from the device the
+ * graph was created on; it never synchronises.
+ *
+ * mla_verify_graph_destroy: releases the graph (NULL is accepted).
+ */
+typedef struct mla_verify_graph mla_verify_graph;
+int mla_verify_graph_create(const void *q_lat, const void *q_rope, const void *kv_cache,
+                            const int32_t *block_table, int32_t *seq_lens, const int32_t *tree_parent,
+                            int32_t *n_tree, const int32_t *topk_idx, int topk, float scale, float *out,
+                            float *lse, int max_batch, int max_total_q, int max_tree, int max_seq_len,
+                            int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                            int num_splits, void *workspace, size_t workspace_bytes, cudaStream_t stream,
+                            mla_verify_graph **graph);
+int mla_verify_graph_launch(mla_verify_graph *graph, int batch, cudaStream_t stream);
+int mla_verify_graph_destroy(mla_verify_graph *graph);
+
+/*
  * Measurement hook: while set, every mla_verify_attn call records `begin`
  * immediately before and `end` immediately after the launch of its fused
  * verify kernel, on the call's stream, so the kernel can be timed alone.

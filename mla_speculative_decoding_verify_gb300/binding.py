@@ -37,7 +37,8 @@ EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_split
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
             "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc",
             "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept",
-            "mla_verify_sparse_num_splits", "mla_verify_sparse_workspace_size", "mla_verify_sparse_attn")
+            "mla_verify_sparse_num_splits", "mla_verify_sparse_workspace_size", "mla_verify_sparse_attn",
+            "mla_verify_graph_create", "mla_verify_graph_launch", "mla_verify_graph_destroy")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -95,6 +96,14 @@ def lib() -> ctypes.CDLL:
         L.mla_tree_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz]
         L.mla_tree_kv_accept.restype = i32
         L.mla_tree_kv_accept.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz]
+        L.mla_verify_graph_create.restype = i32
+        L.mla_verify_graph_create.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, vp,
+                                              i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp,
+                                              ctypes.POINTER(vp)]
+        L.mla_verify_graph_launch.restype = i32
+        L.mla_verify_graph_launch.argtypes = [vp, i32, vp]
+        L.mla_verify_graph_destroy.restype = i32
+        L.mla_verify_graph_destroy.argtypes = [vp]
         _lib = L
         return L
 
@@ -314,3 +323,109 @@ def verify_sparse(db: "DeviceBatch", topk_idx, num_splits_req: int = 0, out=None
                              num_splits_req, workspace.data_ptr(), workspace.numel()), "mla_verify_sparse_attn")
     return out, lse, workspace
 
+
+
+def verify_graph_create(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, topk_idx, topk,
+                        scale, out, lse, max_batch, max_total_q, max_tree, max_seq_len, num_heads, page_size,
+                        num_pages, max_pages_per_seq, num_splits, workspace, workspace_bytes, stream):
+    """Raw call; returns (status, handle or None)."""
+    h = ctypes.c_void_p()
+    code = int(lib().mla_verify_graph_create(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree,
+                                             topk_idx, topk, float(scale), out, lse, max_batch, max_total_q,
+                                             max_tree, max_seq_len, num_heads, page_size, num_pages,
+                                             max_pages_per_seq, num_splits, workspace, workspace_bytes, stream,
+                                             ctypes.byref(h)))
+    return code, (h.value if code == MLA_OK else None)
+
+
+def verify_graph_launch(handle, batch, stream) -> int:
+    return int(lib().mla_verify_graph_launch(handle, int(batch), stream))
+
+
+def verify_graph_destroy(handle) -> int:
+    return int(lib().mla_verify_graph_destroy(handle))
+
+
+class VerifyGraph:
+    """A verify step captured once for a bucket of at most `max_batch` requests
+    and `max_total_q` tree tokens over one paged KV cache (mla_verify_graph_*).
+
+    It owns the bucket's input and output buffers on the device: `load()`
+    copies one step's inputs (a VerifyInputs over the same cache) into them,
+    `launch()` replays the graph, padding the requests past the step's batch.
+    `out` / `lse` rows past the step's tree tokens are not defined."""
+
+    def __init__(self, kv_cache, max_batch, max_total_q, max_tree, max_seq_len, page_size, max_pages_per_seq,
+                 scale, topk=0, num_splits_req=0, stream=None):
+        import torch
+        dev = kv_cache.device
+        self.device = dev
+        self.max_batch, self.max_total_q, self.topk = int(max_batch), int(max_total_q), int(topk)
+        self.kv_cache = kv_cache
+        self.q_lat = torch.zeros((max_total_q, NUM_HEADS, D_LATENT), dtype=torch.int16, device=dev)
+        self.q_rope = torch.zeros((max_total_q, NUM_HEADS, D_ROPE), dtype=torch.int16, device=dev)
+        self.block_table = torch.full((max_batch, max_pages_per_seq), -1, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+        self.n_tree = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+        self.tree_parent = torch.full((max_total_q,), -1, dtype=torch.int32, device=dev)
+        self.topk_idx = (torch.full((max_total_q, topk), -1, dtype=torch.int32, device=dev) if topk
+                         else None)
+        self.out = torch.empty((max_total_q, NUM_HEADS, D_LATENT), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((max_total_q, NUM_HEADS), dtype=torch.float32, device=dev)
+        if topk:
+            need = sparse_workspace_size(max_batch, max_total_q, max_tree, topk, NUM_HEADS, num_splits_req)
+        else:
+            need = workspace_size(max_batch, max_total_q, max_tree, max_seq_len, NUM_HEADS, num_splits_req)
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        page_rows = int(kv_cache.shape[0])
+        code, self.handle = verify_graph_create(
+            self.q_lat.data_ptr(), self.q_rope.data_ptr(), kv_cache.data_ptr(), self.block_table.data_ptr(),
+            self.seq_lens.data_ptr(), self.tree_parent.data_ptr(), self.n_tree.data_ptr(),
+            self.topk_idx.data_ptr() if topk else None, self.topk, scale, self.out.data_ptr(),
+            self.lse.data_ptr(), self.max_batch, self.max_total_q, max_tree, max_seq_len, NUM_HEADS, page_size,
+            page_rows, max_pages_per_seq, num_splits_req, self.workspace.data_ptr(), self.workspace.numel(),
+            self.stream.cuda_stream)
+        check(code, "mla_verify_graph_create")
+        self.batch = 0
+        self.total_q = 0
+
+    def load(self, inp, topk_idx=None, non_blocking=False) -> None:
+        """Copy one step's inputs (host VerifyInputs over the graph's cache) into the buffers."""
+        import numpy as np
+        import torch
+        if inp.batch > self.max_batch or inp.total_q > self.max_total_q:
+            raise ValueError("step exceeds the graph's bucket")
+        if inp.max_pages_per_seq > self.block_table.shape[1]:
+            raise ValueError("block table wider than the graph's")
+
+        def put(dst, a, dtype):
+            src = torch.from_numpy(np.ascontiguousarray(a).view(dtype))
+            dst.copy_(src.reshape(dst.shape), non_blocking=non_blocking)
+        nq, b = inp.total_q, inp.batch
+        with torch.cuda.stream(self.stream):
+            put(self.q_lat[:nq], inp.q_lat, np.int16)
+            put(self.q_rope[:nq], inp.q_rope, np.int16)
+            self.block_table[:b].fill_(-1)
+            put(self.block_table[:b, :inp.max_pages_per_seq], inp.block_table, np.int32)
+            put(self.seq_lens[:b], inp.seq_lens, np.int32)
+            put(self.n_tree[:b], inp.n_tree, np.int32)
+            put(self.tree_parent[:nq], inp.tree_parent, np.int32)
+            if self.topk:
+                put(self.topk_idx[:nq], topk_idx, np.int32)
+        self.batch, self.total_q = b, nq
+
+    def launch(self, batch=None) -> None:
+        check(verify_graph_launch(self.handle, self.batch if batch is None else batch, self.stream.cuda_stream),
+              "mla_verify_graph_launch")
+
+    def close(self) -> None:
+        if self.handle is not None:
+            check(verify_graph_destroy(self.handle), "mla_verify_graph_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

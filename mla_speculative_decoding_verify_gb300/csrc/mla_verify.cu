@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "mla_verify.h"
 #include "combine_kernel.cuh"
@@ -226,7 +227,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
                        float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
                        int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
                        int num_splits, void* workspace, size_t workspace_bytes, const int32_t* topk_idx,
-                       int topk) {
+                       int topk, bool graph_capture = false) {
     // ---- host-checkable arguments ----
     if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
         num_splits < 0 || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
@@ -286,6 +287,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.num_pages = num_pages;
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
+    pp.allow_unused_rows = graph_capture ? 1 : 0;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0) {
@@ -328,13 +330,14 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.topk = topk;
     vp.kv = static_cast<const uint16_t*>(kv_cache);
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
-    if (g_prof_begin && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    const bool prof = !graph_capture && g_prof_begin && g_prof_end;
+    if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0)
         mla::mla_verify_kernel<true><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     else
         mla::mla_verify_kernel<false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-    if (g_prof_end && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (prof && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
     // ---- merge of the split partials ----
     if (splits > 1)
@@ -470,4 +473,88 @@ int mla_read_status(const void* workspace, int* device_status) {
     return MLA_OK;
 }
 
+// ---------------------------------------------------------------- graph replay
+
+struct mla_verify_graph {
+    cudaGraphExec_t exec = nullptr;
+    int device = -1;
+    int max_batch = 0;
+    int32_t* seq_lens = nullptr;
+    int32_t* n_tree = nullptr;
+};
+
+int mla_verify_graph_create(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,
+                            int32_t* seq_lens, const int32_t* tree_parent, int32_t* n_tree, const int32_t* topk_idx,
+                            int topk, float scale, float* out, float* lse, int max_batch, int max_total_q,
+                            int max_tree, int max_seq_len, int num_heads, int page_size, int num_pages,
+                            int max_pages_per_seq, int num_splits, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream, mla_verify_graph** graph) {
+    if (!graph) return MLA_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (max_batch <= 0 || max_total_q <= 0 || !seq_lens || !n_tree || topk < 0) return MLA_ERR_INVALID_ARG;
+    if (topk > MLA_MAX_TOPK) return MLA_ERR_UNSUPPORTED;
+    if (topk > 0 && !topk_idx) return MLA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MLA_ERR_NOT_INITIALIZED;
+    // the legacy and per-thread default streams cannot be captured: use a private one
+    cudaStream_t cap = stream, own = nullptr;
+    if (stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread) {
+        if (cudaStreamCreateWithFlags(&own, cudaStreamNonBlocking) != cudaSuccess) return MLA_ERR_CUDA;
+        cap = own;
+    }
+    cudaGraph_t def = nullptr;
+    int rc = MLA_OK;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = MLA_ERR_CUDA;
+    } else {
+        rc = verify_impl(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, out, lse, cap,
+                         max_batch, max_total_q, max_tree, max_seq_len, num_heads, page_size, num_pages,
+                         max_pages_per_seq, num_splits, workspace, workspace_bytes, topk > 0 ? topk_idx : nullptr,
+                         topk, true);
+        const cudaError_t e = cudaStreamEndCapture(cap, &def);
+        if (rc == MLA_OK && e != cudaSuccess) rc = MLA_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (rc == MLA_OK && cudaGraphInstantiate(&exec, def, 0) != cudaSuccess) rc = MLA_ERR_CUDA;
+    if (def) cudaGraphDestroy(def);
+    if (own) cudaStreamDestroy(own);
+    mla_verify_graph* g = rc == MLA_OK ? new (std::nothrow) mla_verify_graph : nullptr;
+    if (rc == MLA_OK && !g) rc = MLA_ERR_CUDA;
+    if (rc != MLA_OK) {
+        if (exec) cudaGraphExecDestroy(exec);
+        return rc;
+    }
+    g->exec = exec;
+    g->device = dev;
+    g->max_batch = max_batch;
+    g->seq_lens = seq_lens;
+    g->n_tree = n_tree;
+    *graph = g;
+    return MLA_OK;
+}
+
+int mla_verify_graph_launch(mla_verify_graph* graph, int batch, cudaStream_t stream) {
+    if (!graph || !graph->exec || batch < 0 || batch > graph->max_batch) return MLA_ERR_INVALID_ARG;
+    if (current_device() != graph->device) return MLA_ERR_INVALID_ARG;
+    if (batch < graph->max_batch) {
+        // requests past `batch` become empty: no tree tokens, no keys, no work items
+        const size_t bytes = sizeof(int32_t) * static_cast<size_t>(graph->max_batch - batch);
+        if (cudaMemsetAsync(graph->n_tree + batch, 0, bytes, stream) != cudaSuccess ||
+            cudaMemsetAsync(graph->seq_lens + batch, 0, bytes, stream) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
+    return cudaGraphLaunch(graph->exec, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_verify_graph_destroy(mla_verify_graph* graph) {
+    if (!graph) return MLA_OK;
+    if (graph->exec && cudaGraphExecDestroy(graph->exec) != cudaSuccess) {
+        delete graph;
+        return MLA_ERR_CUDA;
+    }
+    delete graph;
+    return MLA_OK;
+}
+
 }  // extern "C"
+

@@ -32,6 +32,7 @@ struct PrepParams {
     int* status;                 // [1]
     int batch, total_q, page_size, max_pages, num_pages, max_items;
     int32_t* tok_req;            // sparse variant: [total_q] request of each tree token (-1 if malformed), else null
+    int allow_unused_rows;       // graph replay: sum(n_tree) may be below total_q; the trailing rows are unused
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
 
     // 1. query offsets (exclusive scan of n_tree)
     block_exclusive_scan(p.batch, [&](int b) { return p.n_tree[b]; }, p.q_off, warp_sums);
-    if (tid == 0 && p.q_off[p.batch] != p.total_q) atomicOr(p.status, kStatusBadTree);
+    if (tid == 0 && (p.allow_unused_rows ? p.q_off[p.batch] > p.total_q : p.q_off[p.batch] != p.total_q))
+        atomicOr(p.status, kStatusBadTree);
 
     // 2. one warp per request: validate sizes, parents and block ids, then the
     //    ancestor bit sets by pointer jumping (6 rounds cover depth 64)

@@ -142,6 +142,17 @@ class VerifyInputs:
                                       self.tree_parent, self.n_tree))
 
 
+def first_requests(inp: VerifyInputs, k: int) -> VerifyInputs:
+    """The first k requests of `inp`, sharing its KV cache (same pages and block
+    table rows): smaller batches of one cache, as a serving loop sees them."""
+    k = int(k)
+    nq = int(inp.q_offsets[k])
+    return dataclasses.replace(
+        inp, name=f"{inp.name}[:{k}]", q_lat=inp.q_lat[:nq], q_rope=inp.q_rope[:nq],
+        block_table=inp.block_table[:k], seq_lens=inp.seq_lens[:k], tree_parent=inp.tree_parent[:nq],
+        n_tree=inp.n_tree[:k])
+
+
 # ---------------------------------------------------------------- draft trees
 
 def _tree(kind: str, n: int, rng: np.random.Generator) -> np.ndarray:

@@ -145,3 +145,36 @@ def test_sparse_split_choice_and_workspace(lib):
     assert binding.sparse_num_splits(16, 512, 32, 512, requested=3) == 3
     assert binding.sparse_workspace_size(16, 512, 32, 512) > 0
     assert binding.lib().mla_verify_sparse_num_splits(1, 1, 1, 0, 64, 0) < 0
+
+
+def _graph_create(**over):
+    args = dict(q_lat=16, q_rope=16, kv_cache=16, block_table=16, seq_lens=16, tree_parent=16, n_tree=16,
+                topk_idx=None, topk=0, scale=0.07, out=16, lse=16, max_batch=1, max_total_q=1, max_tree=1,
+                max_seq_len=65, num_heads=64, page_size=64, num_pages=2, max_pages_per_seq=2, num_splits=0,
+                workspace=256, workspace_bytes=1 << 20, stream=None)
+    args.update(over)
+    return binding.verify_graph_create(**args)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(max_batch=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(max_total_q=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(n_tree=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(seq_lens=None), binding.MLA_ERR_INVALID_ARG),
+    (dict(topk=-1), binding.MLA_ERR_INVALID_ARG),
+    (dict(topk=binding.MAX_TOPK + 1), binding.MLA_ERR_UNSUPPORTED),
+    (dict(topk=64), binding.MLA_ERR_INVALID_ARG),            # no slot array
+])
+def test_graph_create_host_checks(lib, over, code):
+    got, handle = _graph_create(**over)
+    assert got == code and handle is None
+
+
+def test_graph_create_needs_init_and_launch_checks(lib):
+    # without a GPU no device is initialised: nothing is captured
+    got, handle = _graph_create()
+    assert got in (binding.MLA_ERR_NOT_INITIALIZED, binding.MLA_ERR_CUDA) and handle is None
+    assert lib.mla_verify_graph_create(16, 16, 16, 16, 16, 16, 16, None, 0, 0.07, 16, 16, 1, 1, 1, 65, 64, 64,
+                                       2, 2, 0, 256, 1 << 20, None, None) == binding.MLA_ERR_INVALID_ARG
+    assert binding.verify_graph_launch(None, 1, None) == binding.MLA_ERR_INVALID_ARG
+    assert binding.verify_graph_destroy(None) == binding.MLA_OK

@@ -777,16 +777,32 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                              ? p.out + grow * kDLatent + kDLatentHalf * c
                              : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
                                    kDLatentHalf * c;
+            // The rows go out through shared memory so that every store instruction
+            // writes whole 128-byte lines: the thread of a row puts 32 of its values
+            // into the warp's 4 KB tile (swizzled), then each lane stores 16 bytes of
+            // one of four rows.  The P buffers are free here (PV is done).  A warp's
+            // 32 rows belong to one token, so row_valid is warp-uniform.
+            const uint32_t ebuf = p_addr + q4 * 4096;
+            float* wdst = dst - static_cast<long long>(lane) * kDLatent;   // the warp's first row
             for (int part = 0; part < kDLatentHalf / 32; ++part) {
                 uint32_t o[32];
                 tmem_ld32(trow + kTmO + 32 * part, o);
                 tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), __uint_as_float(o[4 * u]) * inv_l,
+                                 __uint_as_float(o[4 * u + 1]) * inv_l, __uint_as_float(o[4 * u + 2]) * inv_l,
+                                 __uint_as_float(o[4 * u + 3]) * inv_l);
+                __syncwarp();
                 if (row_valid) {
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<float4*>(dst + 32 * part + 4 * u) =
-                            make_float4(__uint_as_float(o[4 * u]) * inv_l, __uint_as_float(o[4 * u + 1]) * inv_l,
-                                        __uint_as_float(o[4 * u + 2]) * inv_l, __uint_as_float(o[4 * u + 3]) * inv_l);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = 4 * i + (lane >> 3), u = lane & 7;
+                        const float4 v = ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                        *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) = v;
+                    }
                 }
+                __syncwarp();
             }
             if (row_valid && c == 0) {
                 const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;

@@ -177,6 +177,19 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
     return out != 0;
 }
 
+// ------------------------------------------------------------------ per-thread async copies
+
+// 16-byte global -> shared copy (L2 only); completes asynchronously.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_addr, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bring the 128-byte line holding `gmem` into L2 (no data returned).
 __device__ __forceinline__ void prefetch_l2(const void* gmem) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem));

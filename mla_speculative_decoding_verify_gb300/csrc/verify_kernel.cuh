@@ -518,24 +518,45 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
         // q latent half -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory.
+        // The warp copies its 32 rows with 16-byte async copies, one whole 512-byte
+        // row half per instruction, into its 16 KB slice of the staging and P
+        // buffers (nothing uses them before q_ready); then the thread of each row
+        // moves the row into TMEM.  A warp's rows belong to one token, so row_valid
+        // is warp-uniform; rows of a missing second token are zeros.
         {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + grow * kDLatent + kDLatentHalf * c);
+            const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;  // [32 rows][32 units], unit u of row i at u ^ i
+            const long long row0 = static_cast<long long>(qbase) * kHeads + q4 * 32;
+            if (row_valid) {
+                const uint8_t* lat = reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2;
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i)
+                    cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4), lat + static_cast<long long>(i) * kDLatent * 2 + 16 * lane);
+                const uint8_t* rope = reinterpret_cast<const uint8_t*>(p.q_rope) + (row0 * kDRope + kDRopeHalf * c) * 2;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = 8 * i + (lane >> 2), u = lane & 3, rr = q4 * 32 + row;
+                    cp_async_16(qrope_addr + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4),
+                                rope + static_cast<long long>(row) * kDRope * 2 + 16 * u);
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+            } else {
+                for (int u = 0; u < 4; ++u)
+                    st_shared_v4(qrope_addr + r * 64 + ((u ^ ((r >> 1) & 3)) << 4), 0.f, 0.f, 0.f, 0.f);
+            }
+            __syncwarp();
             for (int part = 0; part < 4; ++part) {
                 uint32_t v[32];
+#pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    uint4 w = row_valid ? __ldg(src + part * 8 + u) : make_uint4(0, 0, 0, 0);
-                    v[4 * u + 0] = w.x;
-                    v[4 * u + 1] = w.y;
-                    v[4 * u + 2] = w.z;
-                    v[4 * u + 3] = w.w;
+                    const float4 w = row_valid ? ld_shared_v4(qbuf + lane * 512 + (((8 * part + u) ^ lane) << 4))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[4 * u + 0] = __float_as_uint(w.x);
+                    v[4 * u + 1] = __float_as_uint(w.y);
+                    v[4 * u + 2] = __float_as_uint(w.z);
+                    v[4 * u + 3] = __float_as_uint(w.w);
                 }
                 tmem_st32(trow + kTmQ + 32 * part, v);
-            }
-            const uint4* rs = reinterpret_cast<const uint4*>(p.q_rope + grow * kDRope + kDRopeHalf * c);
-            for (int u = 0; u < 4; ++u) {
-                uint4 w = row_valid ? __ldg(rs + u) : make_uint4(0, 0, 0, 0);
-                const uint32_t off = r * 64 + ((u ^ ((r >> 1) & 3)) << 4);
-                *reinterpret_cast<uint4*>(smem + kOffQRope + off) = w;
             }
             tmem_wait_st();
             fence_proxy_async_smem();

@@ -50,6 +50,18 @@ def test_edge_prefix_and_trees(prefix, kind):
         assert_close(out, lse, ref_o, ref_l, f"prefix={prefix} kind={kind} splits={splits}")
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_requests_without_tree_tokens(splits):
+    """Requests with no draft tokens (n_tree = 0, prefix only) sit between real
+    ones: they add no rows, and the others keep their offsets and results."""
+    inp = I.make_inputs([100, 500, 64, 0, 700], [5, 0, 3, 0, 9], tree_kind="uniform", seed=8, stream=507)
+    assert inp.total_q == 17
+    ref_o, ref_l = oracle.verify(inp)
+    out, lse, status = run_gpu(inp, splits=splits)
+    assert status == 0
+    assert_close(out, lse, ref_o, ref_l, f"empty trees, splits={splits}")
+
+
 @pytest.mark.parametrize("page_size", [64, 128, 192])
 def test_page_sizes(page_size):
     inp = I.make_inputs([300, 64, 1000], [5, 16, 9], tree_kind="uniform", page_size=page_size,

@@ -34,6 +34,19 @@ def test_sparse_parity_scaled_workloads(cfg, div, cap, topk):
     assert_close(out, lse, ref_o, ref_l, f"cfg{cfg} topk{topk}")
 
 
+def test_sparse_maximum_topk():
+    """topk = MLA_MAX_TOPK: 64 slot tiles per token; the shorter prefix lists
+    every position once and leaves the rest of its slots unused."""
+    inp = I.make_inputs([3000, 1000], [3, 2], tree_kind="forest", seed=6, stream=921)
+    idx = I.topk_indices(inp, binding.MAX_TOPK, seed=7)
+    assert (idx[3:] == -1).sum() == 2 * (binding.MAX_TOPK - 1000)
+    ref_o, ref_l = oracle.verify_sparse(inp, idx)
+    for splits in (0, 4):
+        out, lse, status = run_sparse(inp, idx, splits=splits)
+        assert status == 0
+        assert_close(out, lse, ref_o, ref_l, f"topk=max splits={splits}")
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 5])
 def test_sparse_split_counts(splits):
     inp = I.scaled_config_inputs(3, seed=2, prefix_div=16, batch_cap=3)

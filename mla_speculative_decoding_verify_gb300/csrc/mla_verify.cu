@@ -9,6 +9,10 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <algorithm>
+#include <functional>
+#include <queue>
+#include <vector>
 #include <new>
 
 #include "mla_verify.h"
@@ -83,11 +87,12 @@ int sm_count_of_current() {
     return 152;
 }
 
+constexpr double kUnitOverheadTiles = 6.0;  // per work unit: q load, pipeline fill, epilogue
+
 // Model of the verify time (in KV-tile units of one CTA pair) for `splits`
 // splits: whole waves of (request, row tile, split) units over the SMs,
 // a fixed per-unit cost, and the combine pass when split.
 double model_time(long long units_per_split, int tiles, int splits, int pairs, long long rows) {
-    const double kUnitOverheadTiles = 6.0;  // q load, pipeline fill, epilogue
     const double kTileSeconds = 1.1e-6;     // one 64-key tile of 128 rows on a CTA pair
     const double kCombineBytesPerSecond = 5.0e12;
     const long long units = units_per_split * splits;
@@ -98,10 +103,69 @@ double model_time(long long units_per_split, int tiles, int splits, int pairs, l
     return t;
 }
 
+// Work items of a launch (row tiles of two tree tokens), bounded from the sizes.
+long long items_bound_of(int batch, int total_q, int max_tree) {
+    return std::min<long long>(static_cast<long long>(batch) * ((max_tree + 1) / 2),
+                               (static_cast<long long>(total_q) + batch) / 2);
+}
+
+// With two splits: the first split's share of a work item's tiles, in 1/1024.
+// The CTAs of a launch start in grid order, every first split before any
+// second one.  A greedy list-scheduling model of that order over the CTA pairs
+// (a unit costs its tiles plus kUnitOverheadTiles) picks the cut whose rounds
+// end most evenly: a long first part, and a short second part that fills the
+// last round.  Past eight rounds the tail is small and the halves are kept.
+// The last answer is cached (a serving loop repeats its shapes).
+int first_split_share(long long items, int tiles, int pairs) {
+    if (items <= 0 || tiles < 2 || pairs <= 0 || 2 * items > 8LL * pairs) return 0;
+    static std::mutex mu;
+    static long long c_items = -1;
+    static int c_tiles = -1, c_pairs = -1, c_share = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (c_items == items && c_tiles == tiles && c_pairs == pairs) return c_share;
+    }
+    const double o = kUnitOverheadTiles;
+    auto span = [&](int a) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> q;
+        for (int i = 0; i < pairs; ++i) q.push(0.0);
+        auto put = [&](double w) {
+            const double t = q.top();
+            q.pop();
+            q.push(t + w);
+        };
+        for (long long i = 0; i < items; ++i) put(a + o);
+        for (long long i = 0; i < items; ++i) put(tiles - a + o);
+        double m = 0.0;
+        while (!q.empty()) {
+            m = std::max(m, q.top());
+            q.pop();
+        }
+        return m;
+    };
+    const int half = (tiles + 1) / 2;
+    int best_a = half;
+    double best = span(half);
+    const int step = std::max(1, tiles / 64);
+    for (int a = half + step; a < tiles; a += step) {
+        const double m = span(a);
+        if (m < best - 1e-9) {
+            best = m;
+            best_a = a;
+        }
+    }
+    const int share = best_a == half ? 0 : std::clamp((best_a * 1024 + tiles / 2) / tiles, 1, 1023);
+    std::lock_guard<std::mutex> g(mu);
+    c_items = items;
+    c_tiles = tiles;
+    c_pairs = pairs;
+    c_share = share;
+    return share;
+}
+
 // Split count for requests of up to `tiles` KV tiles per row tile.
 int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
-    const long long items_bound = std::min<long long>(static_cast<long long>(batch) * ((max_tree + 1) / 2),
-                                                      (static_cast<long long>(total_q) + batch) / 2);
+    const long long items_bound = items_bound_of(batch, total_q, max_tree);
     const int pairs = sm_count_of_current() / 2;
     const long long rows = static_cast<long long>(total_q) * MLA_NUM_HEADS;
     const int max_s = std::max(1, std::min(MLA_MAX_SPLITS, tiles / 16));
@@ -323,6 +387,11 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.max_pages = max_pages_per_seq;
     vp.num_pages = num_pages;
     vp.num_splits = splits;
+    vp.split_share = splits == 2 ? first_split_share(items_bound_of(batch, total_q, max_tree),
+                                                     topk > 0 ? sparse_tiles(topk)
+                                                              : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN,
+                                                     sm_count_of_current() / 2)
+                                 : 0;
     vp.max_items = lay.max_items;
     vp.scale_log2 = scale * 1.4426950408889634f;
     vp.timeout_ns = kDefaultTimeoutNs;

@@ -103,6 +103,7 @@ struct VerifyParams {
     float* part_out;            // [num_splits, total_q * 64, 512]
     float* part_lse;            // [num_splits, total_q * 64]
     int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
+    int split_share;            // two splits: the first one's share of a work item's tiles, in 1/1024 (0 = halves)
     float scale_log2;           // softmax scale * log2(e)
     uint64_t timeout_ns;
     // sparse variant only
@@ -135,8 +136,15 @@ static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 __device__ __forceinline__ void raise_status(int* status, int bit) { atomicOr(status, bit); }
 
-// Which KV tiles [t0, t1) split `s` of `S` covers, for a request of n tiles.
-__device__ __forceinline__ void split_range(int n, int s, int S, int& t0, int& t1) {
+// Which KV tiles [t0, t1) split `s` of `S` covers, for a request of n tiles.  With
+// two splits and share > 0 the first split takes share / 1024 of the tiles.
+__device__ __forceinline__ void split_range(int n, int s, int S, int share, int& t0, int& t1) {
+    if (S == 2 && share > 0) {
+        const int a = static_cast<int>(min(static_cast<long long>(n), (static_cast<long long>(n) * share + 512) >> 10));
+        t0 = s == 0 ? 0 : a;
+        t1 = s == 0 ? a : n;
+        return;
+    }
     t0 = static_cast<int>((static_cast<long long>(n) * s) / S);
     t1 = static_cast<int>((static_cast<long long>(n) * (s + 1)) / S);
 }
@@ -190,7 +198,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int n_kv_tiles =
         bad ? 0 : (kSparse ? nA + nB + (T + kBlockN - 1) / kBlockN : (L + kBlockN - 1) / kBlockN);
     int t0, t1;
-    split_range(n_kv_tiles, split, p.num_splits, t0, t1);
+    split_range(n_kv_tiles, split, p.num_splits, p.split_share, t0, t1);
     const int n = t1 - t0;
 
     // rows of this thread (softmax warps only)

@@ -95,14 +95,15 @@ def test_graph_sparse_bucket_matches_eager_bitwise():
     import torch
     full = bucket_inputs(kind="forest")
     idx = I.topk_indices(full, 100, seed=5, unused_frac=0.1, duplicates=True)
-    g = make_graph(full, 2, topk=100)
+    # three splits: with two, the split point follows the launch's sizes (bucket vs batch)
+    g = make_graph(full, 3, topk=100)
     try:
         for k in (6, 3):
             sub = I.first_requests(full, k)
             sidx = idx[:sub.total_q]
             o, l, st = replay(g, sub, sidx)
             assert st == 0
-            eo, el = eager(sub, 2, sidx)
+            eo, el = eager(sub, 3, sidx)
             assert torch.equal(o, eo) and torch.equal(l, el), f"sparse batch {k}"
         ref_o, ref_l = oracle.verify_sparse(sub, sidx)
         assert_close(o.numpy().astype(np.float64), l.numpy().astype(np.float64), ref_o, ref_l, "sparse replay")

@@ -46,7 +46,8 @@ int current_device() {
 
 // Workspace layout shared by the size query and the launch.
 struct Layout {
-    size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, tok_req, total;
+    size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, tok_req, merge_cnt,
+        total;
     int max_items;
 };
 
@@ -70,9 +71,11 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false) 
     const size_t rows = static_cast<size_t>(total_q) * MLA_NUM_HEADS;
     if (num_splits > 1) {
         L.part_out = take(sizeof(float) * rows * MLA_D_LATENT * num_splits);
-        L.part_lse = take(sizeof(float) * rows * num_splits);
+        // two splits are merged in the verify kernel: lse per CTA half, and per-tile counters
+        L.part_lse = take(sizeof(float) * rows * num_splits * (num_splits == 2 ? 2 : 1));
+        L.merge_cnt = num_splits == 2 ? take(sizeof(int32_t) * 4 * static_cast<size_t>(L.max_items)) : 0;
     } else {
-        L.part_out = L.part_lse = 0;
+        L.part_out = L.part_lse = L.merge_cnt = 0;
     }
     L.tok_req = sparse ? take(sizeof(int32_t) * (total_q > 0 ? total_q : 1)) : 0;
     L.total = off;
@@ -352,6 +355,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     pp.allow_unused_rows = graph_capture ? 1 : 0;
+    int32_t* merge_cnt = splits == 2 ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    pp.zero_words = merge_cnt;
+    pp.zero_count = merge_cnt ? 4 * lay.max_items : 0;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0) {
@@ -398,6 +404,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.topk_idx = topk_idx;
     vp.topk = topk;
     vp.kv = static_cast<const uint16_t*>(kv_cache);
+    vp.merge_cnt = merge_cnt;
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -408,8 +415,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (prof && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
-    // ---- merge of the split partials ----
-    if (splits > 1)
+    // ---- merge of the split partials (two splits are merged inside the verify kernel) ----
+    if (splits > 2)
         return launch_combine(part_out, part_lse, splits, static_cast<long long>(total_q) * MLA_NUM_HEADS, out, lse,
                               stream);
     return MLA_OK;

@@ -33,6 +33,8 @@ struct PrepParams {
     int batch, total_q, page_size, max_pages, num_pages, max_items;
     int32_t* tok_req;            // sparse variant: [total_q] request of each tree token (-1 if malformed), else null
     int allow_unused_rows;       // graph replay: sum(n_tree) may be below total_q; the trailing rows are unused
+    int32_t* zero_words;         // words cleared before the verify kernel (its two-split merge counters), or null
+    int zero_count;
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     // 0. sparse variant: no token belongs to a request until step 2 says so
     if (p.tok_req)
         for (int g = tid; g < p.total_q; g += kPrepThreads) p.tok_req[g] = -1;
+    if (p.zero_words)
+        for (int g = tid; g < p.zero_count; g += kPrepThreads) p.zero_words[g] = 0;
 
     // 1. query offsets (exclusive scan of n_tree)
     block_exclusive_scan(p.batch, [&](int b) { return p.n_tree[b]; }, p.q_off, warp_sums);

@@ -73,6 +73,8 @@ static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B
 static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0 && kOffP % 1024 == 0,
               "region alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
+// the two-split merge copies the other split's 128 rows x 1 KB over the stages, q rope and receive buffer
+static_assert(kOffStaging - kOffStages >= kRows * kDLatentHalf * 4, "merge buffer");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // S buffer x at kTmS + 64 * x
@@ -109,6 +111,8 @@ struct VerifyParams {
     // sparse variant only
     const int32_t* topk_idx;    // [total_q, topk] prefix positions, -1 = unused slot
     const uint16_t* kv;         // the cache [num_pages * page_size, 576] (L2 prefetch of gathered rows)
+    // exactly two KV splits: merged in the kernel (else null and a separate combine runs)
+    int32_t* merge_cnt;         // [max_items][2 halves][arrived, written], zeroed by the prep kernel
     int topk;
 };
 
@@ -130,6 +134,7 @@ struct Ctrl {
     int abort;
     int lo_flag[2];
     int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
+    int merge_role;     // two-split merge: 0 = first of the row tile's two units here, 1 = second
     uint32_t slot_mask[kStages][2];  // sparse: bit k of half h set if key 32h + k of the stage's tile is a real slot
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -211,8 +216,135 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int qidx = qbase + tok_local;
     const long long grow = static_cast<long long>(qidx) * kHeads + head;  // global output row
 
+    // ---- two-split merge (softmax warps) ----
+    // With exactly two KV splits the two work units of a row tile meet per CTA
+    // half c: the first to arrive writes its normalised partial and lse and
+    // marks them written; the second waits for the mark, copies the other
+    // split's rows of its half into shared memory in one batch of async copies
+    // (the stages, q rope and receive buffer are free by then), and writes the
+    // merged rows, weighting the splits by their lse and adding them in split
+    // order, so the result does not depend on which unit arrives second.  Rows
+    // leave through the warp's 4 KB tile of the P buffers in whole 128-byte
+    // lines.  own(part, v) fills v[32] with this unit's normalised columns
+    // 32 part .. 32 part + 31 of the thread's row; lse_own is its lse.
+    const long long out_rows = static_cast<long long>(p.total_q) * kHeads;
+    auto two_split_merge = [&](auto&& own, float lse_own) {
+        int32_t* cnt = p.merge_cnt + (item_slot * 2 + static_cast<int>(c)) * 2;
+        float* lse2 = p.part_lse + static_cast<long long>(c) * 2 * out_rows;   // [half][split][row]
+        const uint32_t ebuf = smem_u32(smem + kOffP) + q4 * 4096;
+        const long long wrow = grow - lane;   // the warp's first row
+        named_bar_sync(4, kSoftmaxThreads);
+        if (r == 0) ctl->merge_role = atomicAdd(cnt, 1);
+        named_bar_sync(4, kSoftmaxThreads);
+        const int role = *reinterpret_cast<volatile int*>(&ctl->merge_role);
+        if (role == 0) {
+            float* wdst = p.part_out + (static_cast<long long>(split) * out_rows + wrow) * kDLatent + kDLatentHalf * c;
+            for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                float v[32];
+                own(part, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                                 v[4 * u + 3]);
+                __syncwarp();
+                if (row_valid) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = 4 * i + (lane >> 3), u = lane & 7;
+                        *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) =
+                            ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                    }
+                }
+                __syncwarp();
+            }
+            if (row_valid) lse2[split * out_rows + grow] = lse_own;
+            __threadfence();
+            named_bar_sync(4, kSoftmaxThreads);
+            if (r == 0) atomicExch(cnt + 1, 1);
+            return;
+        }
+        if (r == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (atomicAdd(cnt + 1, 0) == 0) {
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    raise_status(p.status, kStatusTimeout);
+                    break;
+                }
+                __nanosleep(100);
+            }
+        }
+        named_bar_sync(4, kSoftmaxThreads);
+        __threadfence();
+        const int other = split ^ 1;
+        // the other split's 32 rows of this warp, 1 KB each: unit u of row i at u ^ (i & 7)
+        const uint32_t obuf = smem_u32(smem + kOffStages) + q4 * (32 * 1024);
+        if (row_valid) {
+            const float* wsrc =
+                p.part_out + (static_cast<long long>(other) * out_rows + wrow) * kDLatent + kDLatentHalf * c;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int u = lane + 32 * h;
+                    cp_async_16(obuf + i * 1024 + ((u ^ (i & 7)) << 4), wsrc + static_cast<long long>(i) * kDLatent + 4 * u);
+                }
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        const float lse_oth = row_valid ? lse2[other * out_rows + grow] : -INFINITY;
+        const float l0 = split == 0 ? lse_own : lse_oth, l1 = split == 0 ? lse_oth : lse_own;
+        const float m = fmaxf(l0, l1);
+        float lse_tot = -INFINITY, w0 = 0.f, w1 = 0.f;
+        if (m != -INFINITY) {
+            lse_tot = m + __logf(__expf(l0 - m) + __expf(l1 - m));
+            w0 = l0 == -INFINITY ? 0.f : __expf(l0 - lse_tot);
+            w1 = l1 == -INFINITY ? 0.f : __expf(l1 - lse_tot);
+        }
+        float* wdst = p.out + wrow * kDLatent + kDLatentHalf * c;
+        for (int part = 0; part < kDLatentHalf / 32; ++part) {
+            float v[32];
+            own(part, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int uu = 8 * part + u;
+                const float4 t = ld_shared_v4(obuf + lane * 1024 + ((uu ^ (lane & 7)) << 4));
+                const float o4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a0 = split == 0 ? v[4 * u + e] : o4[e], a1 = split == 0 ? o4[e] : v[4 * u + e];
+                    v[4 * u + e] = w0 * a0 + w1 * a1;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                             v[4 * u + 3]);
+            __syncwarp();
+            if (row_valid) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + (lane >> 3), u = lane & 7;
+                    *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) =
+                        ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                }
+            }
+            __syncwarp();
+        }
+        if (row_valid && c == 0) p.lse[grow] = lse_tot;
+    };
+
     if (n <= 0) {
         // Empty split or invalid request: normalised output 0, lse -inf.
+        if (p.merge_cnt != nullptr) {
+            if (softmax_warp)
+                two_split_merge([](int, float* v) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = 0.f;
+                }, -INFINITY);
+            return;
+        }
         if (row_valid) {
             float* dst = (p.num_splits == 1)
                              ? p.out + grow * kDLatent + kDLatentHalf * c
@@ -790,7 +922,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 
         // ---- epilogue ----
         if (ok) ok = mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, lim);
-        ok = __all_sync(0xffffffffu, ok);
+        // one decision for all 128 softmax threads (the two-split merge synchronises them)
+        ok = named_bar_and(4, kSoftmaxThreads, ok);
         if (!ok) {
             if (r == 0) {
                 raise_status(p.status, kStatusTimeout);
@@ -799,6 +932,17 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
+        } else if (p.merge_cnt != nullptr) {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
+            two_split_merge([&](int part, float* v) {
+                uint32_t o[32];
+                tmem_ld32(trow + kTmO + 32 * part, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
+            }, lse2 * 0.6931471805599453f);
         } else {
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;

@@ -119,7 +119,11 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
  *  page_size   rows per page, a multiple of 64
  *  num_pages   pages in kv_cache (block ids must lie in [0, num_pages))
  *  max_pages_per_seq  row stride of block_table
- *  num_splits  KV splits (0 = choose, see mla_verify_num_splits)
+ *  num_splits  KV splits (0 = choose, see mla_verify_num_splits).  With two
+ *              splits the verify kernel merges them itself and the first split
+ *              takes a shape-dependent share of each request's KV tiles (chosen
+ *              so that the work units fill the SMs' rounds evenly); with more,
+ *              a log-sum-exp combine pass follows the verify kernel.
  *  workspace   device scratch of at least mla_verify_workspace_size(...) bytes,
  *              256-byte aligned; it holds the status word, the per-call tree
  *              metadata and, when split, the partial outputs.  Its contents

@@ -27,8 +27,11 @@
 // its ancestor-or-self tree tokens.  A row tile's key sequence is token 0's
 // slots, then token 1's slots, then the tree keys; rows see only their own
 // token's slots.  Two TMA warps gather the rows with four-row tensor gathers
-// into the same swizzled stage layout (empty slots read as zeros) and records
+// into the same swizzled stage layout (empty slots read as zeros) and record
 // which of the tile's 64 slots are real.
+// Split KV: a work unit covers a range of a row tile's KV tiles (with two
+// splits, a host-chosen share for the first); two splits are merged here by
+// the second unit of each row tile to finish, more by a separate combine pass.
 // TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
 #pragma once
 

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import hashlib
 import os
+import re
 
 import numpy as np
 
@@ -77,13 +78,21 @@ def io_bytes(inp) -> dict:
 VERIFY_KERNEL_SOURCES = ("sm103_ptx.cuh", "verify_kernel.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed (string
+    literals in these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(files=VERIFY_KERNEL_SOURCES) -> str:
-    """Hash of the sources the fused verify kernel is compiled from; profile
-    figures taken on other sources are stale."""
+    """Hash of the code the fused verify kernel is compiled from (comments and
+    layout ignored); profile figures taken on other code are stale."""
     here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
     h = hashlib.sha256()
     for name in sorted(files):
-        with open(os.path.join(here, name), "rb") as f:
+        with open(os.path.join(here, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]

@@ -385,6 +385,32 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         }
     }
 
+    // Softmax warps: the query copies (global -> shared, into the staging and P
+    // buffers, which nothing uses yet); the rows move into TMEM after the
+    // set-up.  Each warp copies its 32 rows, one whole 512-byte row half per
+    // instruction (unit u of row i at u ^ i), the rope half straight into its
+    // swizzled slot.  The dense kernel starts them before the set-up; the
+    // sparse one after it, so that they do not delay the first tile's slot and
+    // block-table lookups, which gate its first QK.
+    auto issue_q_copies = [&]() {
+        const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;
+        const uint32_t qrope = smem_u32(smem + kOffQRope);
+        const long long row0 = static_cast<long long>(qbase) * kHeads + q4 * 32;
+        const uint8_t* lat = reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i)
+            cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4), lat + static_cast<long long>(i) * kDLatent * 2 + 16 * lane);
+        const uint8_t* rope = reinterpret_cast<const uint8_t*>(p.q_rope) + (row0 * kDRope + kDRopeHalf * c) * 2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 8 * i + (lane >> 2), u = lane & 3, rr = q4 * 32 + row;
+            cp_async_16(qrope + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4),
+                        rope + static_cast<long long>(row) * kDRope * 2 + 16 * u);
+        }
+        cp_async_commit();
+    };
+    if (!kSparse && softmax_warp && row_valid) issue_q_copies();
+
     // ---- set-up ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -661,27 +687,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
         // q latent half -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory.
-        // The warp copies its 32 rows with 16-byte async copies, one whole 512-byte
-        // row half per instruction, into its 16 KB slice of the staging and P
-        // buffers (nothing uses them before q_ready); then the thread of each row
-        // moves the row into TMEM.  A warp's rows belong to one token, so row_valid
-        // is warp-uniform; rows of a missing second token are zeros.
+        // The warp's async copies land in its 16 KB slice of the staging and P
+        // buffers (nothing uses them before q_ready);
+        // then the thread of each row moves the row into TMEM.  A warp's rows
+        // belong to one token, so row_valid is warp-uniform; rows of a missing
+        // second token are zeros.
         {
-            const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;  // [32 rows][32 units], unit u of row i at u ^ i
-            const long long row0 = static_cast<long long>(qbase) * kHeads + q4 * 32;
+            const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;
             if (row_valid) {
-                const uint8_t* lat = reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2;
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i)
-                    cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4), lat + static_cast<long long>(i) * kDLatent * 2 + 16 * lane);
-                const uint8_t* rope = reinterpret_cast<const uint8_t*>(p.q_rope) + (row0 * kDRope + kDRopeHalf * c) * 2;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = 8 * i + (lane >> 2), u = lane & 3, rr = q4 * 32 + row;
-                    cp_async_16(qrope_addr + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4),
-                                rope + static_cast<long long>(row) * kDRope * 2 + 16 * u);
-                }
-                cp_async_commit();
+                if constexpr (kSparse) issue_q_copies();
                 cp_async_wait<0>();
             } else {
                 for (int u = 0; u < 4; ++u)

@@ -91,6 +91,7 @@ int sm_count_of_current() {
 }
 
 constexpr double kUnitOverheadTiles = 6.0;  // per work unit: q load, pipeline fill, epilogue
+constexpr double kMergeTiles = 6.0;         // extra for a second-split unit: the in-kernel merge
 
 // Model of the verify time (in KV-tile units of one CTA pair) for `splits`
 // splits: whole waves of (request, row tile, split) units over the SMs,
@@ -117,7 +118,10 @@ long long items_bound_of(int batch, int total_q, int max_tree) {
 // second one.  A greedy list-scheduling model of that order over the CTA pairs
 // (a unit costs its tiles plus kUnitOverheadTiles) picks the cut whose rounds
 // end most evenly: a long first part, and a short second part that fills the
-// last round.  Past eight rounds the tail is small and the halves are kept.
+// last round.  A second-split unit also carries the merge (kMergeTiles, fitted
+// to a sweep of the share on a 16 x 16384-token batch, where the model's best
+// cut matched the measured one).  Past eight rounds the tail is small and the
+// halves are kept.
 // The last answer is cached (a serving loop repeats its shapes).
 int first_split_share(long long items, int tiles, int pairs) {
     if (items <= 0 || tiles < 2 || pairs <= 0 || 2 * items > 8LL * pairs) return 0;
@@ -138,7 +142,7 @@ int first_split_share(long long items, int tiles, int pairs) {
             q.push(t + w);
         };
         for (long long i = 0; i < items; ++i) put(a + o);
-        for (long long i = 0; i < items; ++i) put(tiles - a + o);
+        for (long long i = 0; i < items; ++i) put(tiles - a + o + kMergeTiles);
         double m = 0.0;
         while (!q.empty()) {
             m = std::max(m, q.top());

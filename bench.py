@@ -237,20 +237,21 @@ def run_ours(args, ranks: Ranks):
     else:
         splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
                                     args.splits)
+    req = args.splits or 0   # 0: the library chooses (and may cut the last round's work items in two)
     out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
-    ws_bytes = (binding.sparse_workspace_size(inp.batch, inp.total_q, inp.max_tree, args.topk, inp.num_heads, splits)
+    ws_bytes = (binding.sparse_workspace_size(inp.batch, inp.total_q, inp.max_tree, args.topk, inp.num_heads, req)
                 if sparse else binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
-                                                      inp.num_heads, splits))
+                                                      inp.num_heads, req))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         if sparse:
-            binding.verify_sparse(db, d_topk, splits, out=out, lse=lse, workspace=ws, stream=stream)
+            binding.verify_sparse(db, d_topk, req, out=out, lse=lse, workspace=ws, stream=stream)
         else:
-            binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
+            binding.verify(db, req, out=out, lse=lse, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -361,10 +362,10 @@ def run_ours(args, ranks: Ranks):
             if i >= 2:
                 stream.wait_event(st_["returned"])  # step i - 2's result has left the device
             if sparse:
-                binding.verify_sparse(st_["db"], st_["topk"], splits, out=st_["out"], lse=st_["lse"],
+                binding.verify_sparse(st_["db"], st_["topk"], req, out=st_["out"], lse=st_["lse"],
                                       workspace=st_["ws"], stream=stream)
             else:
-                binding.verify(st_["db"], splits, out=st_["out"], lse=st_["lse"], workspace=st_["ws"],
+                binding.verify(st_["db"], req, out=st_["out"], lse=st_["lse"], workspace=st_["ws"],
                                stream=stream)
             st_["computed"].record(stream)
 
@@ -610,20 +611,20 @@ def run_graph(args, ranks: Ranks):
     inp = I.config_inputs(WORKLOADS[args.workload], seed=args.seed)
     flops = metrics.algorithmic_flops(inp)
     db = binding.DeviceBatch(inp, dev)
-    splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
-                                args.splits or 0)
+    req = args.splits or 0   # 0: the library chooses
+    splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads, req)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
     ws = torch.empty(binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads,
-                                            splits), dtype=torch.uint8, device=dev)
+                                            req), dtype=torch.uint8, device=dev)
     g = binding.VerifyGraph(db.kv_cache, inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.page_size,
-                            inp.max_pages_per_seq, inp.scale, num_splits_req=splits, stream=stream)
+                            inp.max_pages_per_seq, inp.scale, num_splits_req=req, stream=stream)
     g.load(inp)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def eager():
-        binding.verify(db, splits, out=out, lse=lse, workspace=ws, stream=stream)
+        binding.verify(db, req, out=out, lse=lse, workspace=ws, stream=stream)
 
     def replay():
         g.launch()

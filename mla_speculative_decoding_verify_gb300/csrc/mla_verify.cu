@@ -51,7 +51,30 @@ struct Layout {
     int max_items;
 };
 
-Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false) {
+// One split chosen automatically: the work items of the last, partial round of
+// CTA pairs (rem = items mod pairs, when at most half the pairs) are cut in
+// two and merged in the kernel, so that their halves run side by side and the
+// last round ends about twice as early.  The cut balances the two halves, the
+// second of which also carries the merge (merge_tiles, in KV tiles of the
+// variant).  Items of fewer than 12 tiles are not cut (measured on a 5-tile
+// item: the merge cost more than the halves saved).  Returns k = 0 when not
+// worth it.
+struct TailPlan {
+    int k = 0, share = 0;
+};
+
+TailPlan tail_plan(long long items, int tiles, int pairs, double merge_tiles) {
+    TailPlan t;
+    if (items <= 0 || tiles < 12 || pairs <= 0) return t;   // short items: the merge costs more than it saves
+    const long long rem = items % pairs;
+    if (rem == 0 || 2 * rem > pairs) return t;
+    const int a = std::clamp(static_cast<int>(std::lround((tiles + merge_tiles) / 2.0)), (tiles + 1) / 2, tiles - 1);
+    t.k = static_cast<int>(rem);
+    t.share = std::clamp((a * 1024 + tiles / 2) / tiles, 1, 1023);
+    return t;
+}
+
+Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, int tail_k = 0) {
     Layout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -59,7 +82,7 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false) 
         off = align_up(off + bytes, 256);
         return at;
     };
-    L.max_items = (total_q + batch) / 2 + 1;
+    L.max_items = (total_q + batch) / 2 + 1 + tail_k;   // + the extra units of cut tail items
     L.status = take(sizeof(int));
     L.item_count = take(sizeof(int));
     L.q_off = take(sizeof(int32_t) * (batch + 1));
@@ -69,7 +92,8 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false) 
     L.anc = take(sizeof(uint64_t) * (total_q > 0 ? total_q : 1));
     L.items = take(sizeof(int2) * L.max_items);
     const size_t rows = static_cast<size_t>(total_q) * MLA_NUM_HEADS;
-    if (num_splits > 1) {
+    if (num_splits > 1 || tail_k > 0) {
+        num_splits = std::max(num_splits, 2);
         L.part_out = take(sizeof(float) * rows * MLA_D_LATENT * num_splits);
         // two splits are merged in the verify kernel: lse per CTA half, and per-tile counters
         L.part_lse = take(sizeof(float) * rows * num_splits * (num_splits == 2 ? 2 : 1));
@@ -195,6 +219,14 @@ int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
 // KV tiles of a sparse row tile: two tokens' slot lists, then the tree keys.
 int sparse_tiles(int topk) { return 2 * ((topk + mla::kBlockN - 1) / mla::kBlockN) + 1; }
 
+// Tail cut of a launch whose split count was chosen automatically as one (an
+// explicit request is taken as it is).  `tiles` = KV tiles of a work item.
+TailPlan launch_tail_plan(bool sparse, int batch, int total_q, int max_tree, int tiles, int requested, int splits) {
+    if (requested != 0 || splits != 1) return TailPlan{};
+    return tail_plan(items_bound_of(batch, total_q, max_tree), tiles, sm_count_of_current() / 2,
+                     sparse ? 2.0 : kMergeTiles);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Maps over the cache as a [rows, 576] bf16 tensor: 64-dim latent chunks (128B
@@ -267,12 +299,13 @@ int mla_init(int device) {
     if (cudaFuncSetAttribute(mla::mla_tree_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(mla::kAcceptSmemBytes)) != cudaSuccess)
         return MLA_ERR_CUDA;
-    if (cudaFuncSetAttribute(mla::mla_verify_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
-        return MLA_ERR_CUDA;
-    if (cudaFuncSetAttribute(mla::mla_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(mla::kSmemBytes)) != cudaSuccess)
-        return MLA_ERR_CUDA;
+    for (const void* fn : {reinterpret_cast<const void*>(mla::mla_verify_kernel<false, false>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<false, true>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, false>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, true>)})
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mla::kSmemBytes)) !=
+            cudaSuccess)
+            return MLA_ERR_CUDA;
     g_dev[device].sm_count = prop.multiProcessorCount;
     g_dev[device].ready = true;
     return MLA_OK;
@@ -289,7 +322,9 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
                                  int num_splits) {
     const int s = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (s <= 0) return 0;
-    return make_layout(batch, total_q, s).total;
+    const TailPlan tp = launch_tail_plan(false, batch, total_q, max_tree,
+                                         (max_seq_len + mla::kBlockN - 1) / mla::kBlockN, num_splits, s);
+    return make_layout(batch, total_q, s, false, tp.k).total;
 }
 
 // Both entry points: topk == 0 is the dense verify, topk > 0 the sparse variant.
@@ -318,7 +353,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     const int splits = topk > 0 ? mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits)
                                 : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (splits <= 0) return MLA_ERR_INVALID_ARG;
-    const Layout lay = make_layout(batch, total_q, splits, topk > 0);
+    const int item_tiles = topk > 0 ? sparse_tiles(topk) : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
+    const TailPlan tail = launch_tail_plan(topk > 0, batch, total_q, max_tree, item_tiles, num_splits, splits);
+    const Layout lay = make_layout(batch, total_q, splits, topk > 0, tail.k);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_WORKSPACE;
 
@@ -329,8 +366,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     int32_t* req_state = reinterpret_cast<int32_t*>(ws + lay.req_state);
     uint64_t* anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
     int2* items = reinterpret_cast<int2*>(ws + lay.items);
-    float* part_out = splits > 1 ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
-    float* part_lse = splits > 1 ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+    float* part_out = (splits > 1 || tail.k > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
+    float* part_lse = (splits > 1 || tail.k > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
 
     CUtensorMap map_lat, map_rope;
     const int enc = encode_maps(kv_cache, static_cast<long long>(num_pages) * page_size,
@@ -359,7 +396,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     pp.allow_unused_rows = graph_capture ? 1 : 0;
-    int32_t* merge_cnt = splits == 2 ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    int32_t* merge_cnt = (splits == 2 || tail.k > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
     pp.zero_words = merge_cnt;
     pp.zero_count = merge_cnt ? 4 * lay.max_items : 0;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
@@ -397,11 +434,11 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.max_pages = max_pages_per_seq;
     vp.num_pages = num_pages;
     vp.num_splits = splits;
-    vp.split_share = splits == 2 ? first_split_share(items_bound_of(batch, total_q, max_tree),
-                                                     topk > 0 ? sparse_tiles(topk)
-                                                              : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN,
+    vp.split_share = splits == 2 ? first_split_share(items_bound_of(batch, total_q, max_tree), item_tiles,
                                                      sm_count_of_current() / 2)
                                  : 0;
+    vp.tail_split = tail.k;
+    vp.tail_share = tail.share;
     vp.max_items = lay.max_items;
     vp.scale_log2 = scale * 1.4426950408889634f;
     vp.timeout_ns = kDefaultTimeoutNs;
@@ -412,10 +449,15 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
-    if (topk > 0)
-        mla::mla_verify_kernel<true><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    const bool merge = merge_cnt != nullptr;
+    if (topk > 0 && merge)
+        mla::mla_verify_kernel<true, true><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    else if (topk > 0)
+        mla::mla_verify_kernel<true, false><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+    else if (merge)
+        mla::mla_verify_kernel<false, true><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     else
-        mla::mla_verify_kernel<false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
+        mla::mla_verify_kernel<false, false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (prof && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
@@ -447,7 +489,8 @@ size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, in
                                         int num_splits) {
     const int s = mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits);
     if (s <= 0) return 0;
-    return make_layout(batch, total_q, s, true).total;
+    const TailPlan tp = launch_tail_plan(true, batch, total_q, max_tree, sparse_tiles(topk), num_splits, s);
+    return make_layout(batch, total_q, s, true, tp.k).total;
 }
 
 int mla_verify_sparse_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,

@@ -109,6 +109,8 @@ struct VerifyParams {
     float* part_lse;            // [num_splits, total_q * 64]
     int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
     int split_share;            // two splits: the first one's share of a work item's tiles, in 1/1024 (0 = halves)
+    // one split, but the last tail_split work items cut in two (tail_share for the first part) and merged
+    int tail_split, tail_share;
     float scale_log2;           // softmax scale * log2(e)
     uint64_t timeout_ns;
     // sparse variant only
@@ -172,7 +174,9 @@ __device__ __forceinline__ void sparse_segment(int j, int nA, int nB, int& kind,
     }
 }
 
-template <bool kSparse>
+// kMerge: the variant that can merge two splits in the kernel (its code is
+// kept out of the plain variant: small launches run every path cold).
+template <bool kSparse, bool kMerge>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
 mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap map_lat,
                   const __grid_constant__ CUtensorMap map_rope) {
@@ -184,11 +188,26 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t peer = c ^ 1u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int item_slot = blockIdx.x >> 1;
-    const int split = blockIdx.y;
+    // ---- work unit: (work item, split of it, splits of it) ----
+    // Regular: one unit per (item, blockIdx.y).  With tail_split = k > 0 the
+    // whole items come first, then the first parts of the last k items, then
+    // their second parts.
+    const int n_items = __ldg(p.item_count);
+    int item_slot = blockIdx.x >> 1, split = blockIdx.y, nsplit = p.num_splits, share = p.split_share;
+    if (p.tail_split > 0) {
+        const int k = min(p.tail_split, n_items), whole = n_items - k;
+        if (item_slot >= whole) {
+            const int j = item_slot - whole;
+            if (j >= 2 * k) return;
+            item_slot = whole + j % k;
+            split = j / k;
+            nsplit = 2;
+            share = p.tail_share;
+        }
+    }
 
     // ---- work item (identical in both CTAs of the pair) ----
-    if (item_slot >= __ldg(p.item_count)) return;
+    if (item_slot >= n_items) return;
     const int2 item = p.items[item_slot];
     const int b = item.x;
     const int tile = item.y;
@@ -206,7 +225,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int n_kv_tiles =
         bad ? 0 : (kSparse ? nA + nB + (T + kBlockN - 1) / kBlockN : (L + kBlockN - 1) / kBlockN);
     int t0, t1;
-    split_range(n_kv_tiles, split, p.num_splits, p.split_share, t0, t1);
+    split_range(n_kv_tiles, split, nsplit, share, t0, t1);
+    const bool merge2 = kMerge && p.merge_cnt != nullptr && nsplit == 2;
     const int n = t1 - t0;
 
     // rows of this thread (softmax warps only)
@@ -340,7 +360,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 
     if (n <= 0) {
         // Empty split or invalid request: normalised output 0, lse -inf.
-        if (p.merge_cnt != nullptr) {
+        if (merge2) {
             if (softmax_warp)
                 two_split_merge([](int, float* v) {
 #pragma unroll
@@ -349,14 +369,14 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             return;
         }
         if (row_valid) {
-            float* dst = (p.num_splits == 1)
+            float* dst = (nsplit == 1)
                              ? p.out + grow * kDLatent + kDLatentHalf * c
                              : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
                                    kDLatentHalf * c;
             for (int d = 0; d < kDLatentHalf; d += 4)
                 *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c == 0) {
-                if (p.num_splits == 1) p.lse[grow] = -INFINITY;
+                if (nsplit == 1) p.lse[grow] = -INFINITY;
                 else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = -INFINITY;
             }
         }
@@ -940,7 +960,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // ---- epilogue ----
         if (ok) ok = mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, lim);
         // one decision for all 128 softmax threads (the two-split merge synchronises them)
-        ok = named_bar_and(4, kSoftmaxThreads, ok);
+        if constexpr (kMerge) ok = named_bar_and(4, kSoftmaxThreads, ok);
+        else ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (r == 0) {
                 raise_status(p.status, kStatusTimeout);
@@ -949,7 +970,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
-        } else if (p.merge_cnt != nullptr) {
+        } else if (merge2) {
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
@@ -963,7 +984,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         } else {
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            float* dst = (p.num_splits == 1)
+            float* dst = (nsplit == 1)
                              ? p.out + grow * kDLatent + kDLatentHalf * c
                              : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
                                    kDLatentHalf * c;
@@ -997,7 +1018,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (row_valid && c == 0) {
                 const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
                 const float v = lse2 * 0.6931471805599453f;
-                if (p.num_splits == 1) p.lse[grow] = v;
+                if (nsplit == 1) p.lse[grow] = v;
                 else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = v;
             }
         }

@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace mla {
 
 constexpr int kCombineWarps = 8;
@@ -12,6 +14,7 @@ constexpr int kCombineWarps = 8;
 __global__ void __launch_bounds__(kCombineWarps * 32)
 mla_combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse, int num_splits,
                    long long rows, float* __restrict__ out, float* __restrict__ lse) {
+    grid_dependency_wait();     // the verify kernel's partials
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
     if (row >= rows) return;

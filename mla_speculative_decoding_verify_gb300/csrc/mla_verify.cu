@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <algorithm>
 #include <functional>
 #include <queue>
@@ -248,13 +249,33 @@ int encode_maps(const void* kv_cache, long long rows, unsigned box_rows, CUtenso
     return (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS) ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream: the
+// grid may start while that one finishes and waits (griddepcontrol.wait) before
+// reading its results, which hides the launch latency between the step's kernels.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int launch_combine(const float* part_out, const float* part_lse, int num_splits, long long rows, float* out,
                    float* lse, cudaStream_t stream) {
     if (rows == 0) return MLA_OK;
     const long long blocks = (rows + mla::kCombineWarps - 1) / mla::kCombineWarps;
-    mla::mla_combine_kernel<<<static_cast<unsigned>(blocks), mla::kCombineWarps * 32, 0, stream>>>(
-        part_out, part_lse, num_splits, rows, out, lse);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    const cudaError_t e = launch_dependent(mla::mla_combine_kernel, dim3(static_cast<unsigned>(blocks)),
+                                           dim3(mla::kCombineWarps * 32), 0, stream, part_out, part_lse, num_splits,
+                                           rows, out, lse);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -406,9 +427,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
         const long long want = (entries + 4LL * mla::kCheckThreads - 1) / (4LL * mla::kCheckThreads);
         const unsigned blocks =
             static_cast<unsigned>(std::max(1LL, std::min<long long>(want, 4LL * sm_count_of_current())));
-        mla::mla_topk_check_kernel<<<blocks, mla::kCheckThreads, 0, stream>>>(
-            topk_idx, topk, entries, pp.tok_req, seq_lens, n_tree, batch, req_state, status);
-        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_dependent(mla::mla_topk_check_kernel, dim3(blocks), dim3(mla::kCheckThreads), 0, stream, topk_idx,
+                             topk, entries, pp.tok_req, seq_lens, n_tree, batch, req_state, status) != cudaSuccess)
+            return MLA_ERR_CUDA;
     }
 
     // ---- fused verify attention ----
@@ -450,15 +471,11 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     const bool merge = merge_cnt != nullptr;
-    if (topk > 0 && merge)
-        mla::mla_verify_kernel<true, true><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
-    else if (topk > 0)
-        mla::mla_verify_kernel<true, false><<<grid, mla::kThreadsSparse, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
-    else if (merge)
-        mla::mla_verify_kernel<false, true><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
-    else
-        mla::mla_verify_kernel<false, false><<<grid, mla::kThreads, mla::kSmemBytes, stream>>>(vp, map_lat, map_rope);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    auto* kernel = topk > 0 ? (merge ? mla::mla_verify_kernel<true, true> : mla::mla_verify_kernel<true, false>)
+                            : (merge ? mla::mla_verify_kernel<false, true> : mla::mla_verify_kernel<false, false>);
+    if (launch_dependent(kernel, grid, dim3(topk > 0 ? mla::kThreadsSparse : mla::kThreads), mla::kSmemBytes, stream,
+                         vp, map_lat, map_rope) != cudaSuccess)
+        return MLA_ERR_CUDA;
     if (prof && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
     // ---- merge of the split partials (two splits are merged inside the verify kernel) ----

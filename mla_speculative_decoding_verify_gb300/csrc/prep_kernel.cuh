@@ -73,6 +73,7 @@ __device__ void block_exclusive_scan(int n, F f, int32_t* dst, int32_t* warp_sum
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepParams p) {
+    grid_launch_dependents();   // the verify kernel may start its launch; it waits for this grid's results
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t tree_par[kPrepWarps][kMaxTree];
     __shared__ uint64_t tree_anc[kPrepWarps][kMaxTree];
@@ -218,6 +219,8 @@ __global__ void __launch_bounds__(kCheckThreads) mla_topk_check_kernel(const int
                                                                      long long entries, const int32_t* tok_req,
                                                                      const int32_t* seq_lens, const int32_t* n_tree,
                                                                      int batch, int32_t* req_state, int* status) {
+    grid_dependency_wait();     // the prep kernel's tok_req and req_state
+    grid_launch_dependents();
     for (long long e = blockIdx.x * static_cast<long long>(kCheckThreads) + threadIdx.x; e < entries;
          e += static_cast<long long>(gridDim.x) * kCheckThreads) {
         const int v = __ldg(topk_idx + e);

@@ -209,6 +209,14 @@ __device__ __forceinline__ void prefetch_l2(const void* gmem) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem));
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op without such a launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream, if launched as a dependent, start now.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -192,6 +192,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // Regular: one unit per (item, blockIdx.y).  With tail_split = k > 0 the
     // whole items come first, then the first parts of the last k items, then
     // their second parts.
+    grid_dependency_wait();     // the prep (and slot check) kernels' work list and metadata
+    grid_launch_dependents();
     const int n_items = __ldg(p.item_count);
     int item_slot = blockIdx.x >> 1, split = blockIdx.y, nsplit = p.num_splits, share = p.split_share;
     if (p.tail_split > 0) {

@@ -286,8 +286,9 @@ def run_ours(args, ranks: Ranks):
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     t_step = ranks.max(sum(step_ms) / K, dev)
     t_kern = ranks.max(sum(kern_ms) / K, dev)
-    # prep, the top-k slot check (sparse), the verify kernel, the combine (split KV)
-    launches = (2 + (1 if sparse else 0) + (1 if splits > 1 else 0)) * K
+    # prep, the top-k slot check (sparse), the verify kernel, the combine (more than two splits;
+    # two are merged inside the verify kernel)
+    launches = (2 + (1 if sparse else 0) + (1 if splits > 2 else 0)) * K
 
     # end to end through the public API: pinned host inputs in, results out, every step
     e2e = None
@@ -718,7 +719,7 @@ def run_graph(args, ranks: Ranks):
                      "note": "small batches are launch- and latency-bound; the fraction is context only"},
         "e2e": {"value": lat_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": lat_e2e * 1e-3},
-        "gpu_launches": (2 + (1 if splits > 1 else 0)) * K * 5,   # graph and eager: latency and event loops; e2e
+        "gpu_launches": (2 + (1 if splits > 2 else 0)) * K * 5,   # graph and eager: latency and event loops; e2e
         "clocks": clk,
         "device_status": status,
     }

@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the tree-verify MLA attention path (one JSON line on rank 0).
 
-A step is one call of mla_verify_attn (prep -> fused verify -> split combine)
-over one batch of synthetic inputs resident in HBM.  Default workload: 16
+A step is one call of mla_verify_attn (prep -> fused verify, which merges two
+KV splits itself; a combine pass follows only for more splits) over one batch
+of synthetic inputs resident in HBM.  Default workload: 16
 requests x prefix 16384 x 32-node draft trees, 64 heads, paged KV (page 64,
 random block table) -- the uniform workload at the prefix length where the
 roofline target applies.  ``--workload`` selects another one.
@@ -11,6 +12,7 @@ roofline target applies.  ``--workload`` selects another one.
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
   python bench.py --path append|accept   # the paged-cache steps around verify (GB/s)
   python bench.py --path sparse [--topk 512]   # the sparse (top-k) verify variant
+  python bench.py --path graph --workload c1   # small-batch step latency, CUDA-graph replay vs eager
 
 For N > 1 (torchrun) every rank runs an independent replica of the workload
 on its own GPU (the path has no exchange step); value = all ranks' work over

@@ -140,3 +140,24 @@ def test_graph_launch_host_checks():
         assert binding.read_status(g.workspace.data_ptr()) == 0
     finally:
         g.close()
+
+
+def test_graph_auto_splits_tail_cut_matches_oracle():
+    """Automatic splits on a one-round bucket: its work items are cut in two and
+    merged in the kernel; smaller replays cut at most the items they have."""
+    import torch
+    full = I.make_inputs([1500, 900, 1200, 800], [16, 8, 32, 4], seed=31, tree_kind="uniform", stream=504)
+    assert binding.num_splits(full.batch, full.total_q, full.max_tree, full.max_seq_len) == 1
+    g = make_graph(full, 0)
+    try:
+        for k in (4, 2, 1):
+            sub = I.first_requests(full, k)
+            o, l, st = replay(g, sub)
+            assert st == 0
+            ref_o, ref_l = oracle.verify(sub)
+            assert_close(o.numpy().astype(np.float64), l.numpy().astype(np.float64), ref_o, ref_l, f"batch {k}")
+        eo, el = eager(full, 0)
+        o, l, _ = replay(g, full)
+        assert torch.equal(o, eo) and torch.equal(l, el), "same shape: replay equals eager"
+    finally:
+        g.close()

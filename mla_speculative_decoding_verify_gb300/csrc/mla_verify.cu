@@ -48,34 +48,33 @@ int current_device() {
 // Workspace layout shared by the size query and the launch.
 struct Layout {
     size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, tok_req, merge_cnt,
-        total;
+        tail_k, total;
     int max_items;
 };
 
 // One split chosen automatically: the work items of the last, partial round of
 // CTA pairs (rem = items mod pairs, when at most half the pairs) are cut in
 // two and merged in the kernel, so that their halves run side by side and the
-// last round ends about twice as early.  The cut balances the two halves, the
-// second of which also carries the merge (merge_tiles, in KV tiles of the
+// last round ends about twice as early.  The prep kernel picks rem from the
+// exact item count; the host fixes the cap (half the pairs: the grid's extra
+// units and the partial buffers) and the cut, which balances the two halves,
+// the second of which also carries the merge (merge_tiles, in KV tiles of the
 // variant).  Items of fewer than 12 tiles are not cut (measured on a 5-tile
-// item: the merge cost more than the halves saved).  Returns k = 0 when not
-// worth it.
+// item: the merge cost more than the halves saved).  cap = 0: no cutting.
 struct TailPlan {
-    int k = 0, share = 0;
+    int cap = 0, share = 0;
 };
 
-TailPlan tail_plan(long long items, int tiles, int pairs, double merge_tiles) {
+TailPlan tail_plan(int tiles, int pairs, double merge_tiles) {
     TailPlan t;
-    if (items <= 0 || tiles < 12 || pairs <= 0) return t;   // short items: the merge costs more than it saves
-    const long long rem = items % pairs;
-    if (rem == 0 || 2 * rem > pairs) return t;
+    if (tiles < 12 || pairs < 2) return t;   // short items: the merge costs more than it saves
     const int a = std::clamp(static_cast<int>(std::lround((tiles + merge_tiles) / 2.0)), (tiles + 1) / 2, tiles - 1);
-    t.k = static_cast<int>(rem);
+    t.cap = pairs / 2;
     t.share = std::clamp((a * 1024 + tiles / 2) / tiles, 1, 1023);
     return t;
 }
 
-Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, int tail_k = 0) {
+Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, int tail_cap = 0) {
     Layout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -83,7 +82,7 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, 
         off = align_up(off + bytes, 256);
         return at;
     };
-    L.max_items = (total_q + batch) / 2 + 1 + tail_k;   // + the extra units of cut tail items
+    L.max_items = (total_q + batch) / 2 + 1;
     L.status = take(sizeof(int));
     L.item_count = take(sizeof(int));
     L.q_off = take(sizeof(int32_t) * (batch + 1));
@@ -93,14 +92,19 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, 
     L.anc = take(sizeof(uint64_t) * (total_q > 0 ? total_q : 1));
     L.items = take(sizeof(int2) * L.max_items);
     const size_t rows = static_cast<size_t>(total_q) * MLA_NUM_HEADS;
-    if (num_splits > 1 || tail_k > 0) {
-        num_splits = std::max(num_splits, 2);
+    L.part_out = L.part_lse = L.merge_cnt = L.tail_k = 0;
+    if (num_splits > 1) {
         L.part_out = take(sizeof(float) * rows * MLA_D_LATENT * num_splits);
         // two splits are merged in the verify kernel: lse per CTA half, and per-tile counters
         L.part_lse = take(sizeof(float) * rows * num_splits * (num_splits == 2 ? 2 : 1));
         L.merge_cnt = num_splits == 2 ? take(sizeof(int32_t) * 4 * static_cast<size_t>(L.max_items)) : 0;
-    } else {
-        L.part_out = L.part_lse = L.merge_cnt = 0;
+    } else if (tail_cap > 0) {
+        // cut tail items: partials of up to tail_cap row tiles, compact, two splits
+        const size_t prows = static_cast<size_t>(tail_cap) * mla::kRows;
+        L.part_out = take(sizeof(float) * prows * MLA_D_LATENT * 2);
+        L.part_lse = take(sizeof(float) * prows * 2 * 2);
+        L.merge_cnt = take(sizeof(int32_t) * 4 * static_cast<size_t>(L.max_items));
+        L.tail_k = take(sizeof(int32_t));
     }
     L.tok_req = sparse ? take(sizeof(int32_t) * (total_q > 0 ? total_q : 1)) : 0;
     L.total = off;
@@ -222,10 +226,9 @@ int sparse_tiles(int topk) { return 2 * ((topk + mla::kBlockN - 1) / mla::kBlock
 
 // Tail cut of a launch whose split count was chosen automatically as one (an
 // explicit request is taken as it is).  `tiles` = KV tiles of a work item.
-TailPlan launch_tail_plan(bool sparse, int batch, int total_q, int max_tree, int tiles, int requested, int splits) {
+TailPlan launch_tail_plan(bool sparse, int tiles, int requested, int splits) {
     if (requested != 0 || splits != 1) return TailPlan{};
-    return tail_plan(items_bound_of(batch, total_q, max_tree), tiles, sm_count_of_current() / 2,
-                     sparse ? 2.0 : kMergeTiles);
+    return tail_plan(tiles, sm_count_of_current() / 2, sparse ? 2.0 : kMergeTiles);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -343,9 +346,8 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
                                  int num_splits) {
     const int s = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (s <= 0) return 0;
-    const TailPlan tp = launch_tail_plan(false, batch, total_q, max_tree,
-                                         (max_seq_len + mla::kBlockN - 1) / mla::kBlockN, num_splits, s);
-    return make_layout(batch, total_q, s, false, tp.k).total;
+    const TailPlan tp = launch_tail_plan(false, (max_seq_len + mla::kBlockN - 1) / mla::kBlockN, num_splits, s);
+    return make_layout(batch, total_q, s, false, tp.cap).total;
 }
 
 // Both entry points: topk == 0 is the dense verify, topk > 0 the sparse variant.
@@ -375,8 +377,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
                                 : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (splits <= 0) return MLA_ERR_INVALID_ARG;
     const int item_tiles = topk > 0 ? sparse_tiles(topk) : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
-    const TailPlan tail = launch_tail_plan(topk > 0, batch, total_q, max_tree, item_tiles, num_splits, splits);
-    const Layout lay = make_layout(batch, total_q, splits, topk > 0, tail.k);
+    const TailPlan tail = launch_tail_plan(topk > 0, item_tiles, num_splits, splits);
+    const Layout lay = make_layout(batch, total_q, splits, topk > 0, tail.cap);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_WORKSPACE;
 
@@ -387,8 +389,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     int32_t* req_state = reinterpret_cast<int32_t*>(ws + lay.req_state);
     uint64_t* anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
     int2* items = reinterpret_cast<int2*>(ws + lay.items);
-    float* part_out = (splits > 1 || tail.k > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
-    float* part_lse = (splits > 1 || tail.k > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+    float* part_out = (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
+    float* part_lse = (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+    int32_t* tail_k = tail.cap > 0 ? reinterpret_cast<int32_t*>(ws + lay.tail_k) : nullptr;
 
     CUtensorMap map_lat, map_rope;
     const int enc = encode_maps(kv_cache, static_cast<long long>(num_pages) * page_size,
@@ -417,7 +420,10 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     pp.allow_unused_rows = graph_capture ? 1 : 0;
-    int32_t* merge_cnt = (splits == 2 || tail.k > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    int32_t* merge_cnt = (splits == 2 || tail.cap > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    pp.tail_k = tail_k;
+    pp.tail_cap = tail.cap;
+    pp.pairs = sm_count_of_current() / 2;
     pp.zero_words = merge_cnt;
     pp.zero_count = merge_cnt ? 4 * lay.max_items : 0;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
@@ -458,8 +464,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.split_share = splits == 2 ? first_split_share(items_bound_of(batch, total_q, max_tree), item_tiles,
                                                      sm_count_of_current() / 2)
                                  : 0;
-    vp.tail_split = tail.k;
+    vp.tail_cap = tail.cap;
     vp.tail_share = tail.share;
+    vp.tail_k = tail_k;
     vp.max_items = lay.max_items;
     vp.scale_log2 = scale * 1.4426950408889634f;
     vp.timeout_ns = kDefaultTimeoutNs;
@@ -467,7 +474,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.topk = topk;
     vp.kv = static_cast<const uint16_t*>(kv_cache);
     vp.merge_cnt = merge_cnt;
-    const dim3 grid(2u * static_cast<unsigned>(lay.max_items), static_cast<unsigned>(splits), 1u);
+    const dim3 grid(2u * static_cast<unsigned>(lay.max_items + tail.cap), static_cast<unsigned>(splits), 1u);
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     const bool merge = merge_cnt != nullptr;
@@ -506,8 +513,8 @@ size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, in
                                         int num_splits) {
     const int s = mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits);
     if (s <= 0) return 0;
-    const TailPlan tp = launch_tail_plan(true, batch, total_q, max_tree, sparse_tiles(topk), num_splits, s);
-    return make_layout(batch, total_q, s, true, tp.k).total;
+    const TailPlan tp = launch_tail_plan(true, sparse_tiles(topk), num_splits, s);
+    return make_layout(batch, total_q, s, true, tp.cap).total;
 }
 
 int mla_verify_sparse_attn(const void* q_lat, const void* q_rope, const void* kv_cache, const int32_t* block_table,

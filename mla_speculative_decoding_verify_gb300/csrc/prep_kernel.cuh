@@ -35,6 +35,8 @@ struct PrepParams {
     int allow_unused_rows;       // graph replay: sum(n_tree) may be below total_q; the trailing rows are unused
     int32_t* zero_words;         // words cleared before the verify kernel (its two-split merge counters), or null
     int zero_count;
+    int32_t* tail_k;             // one split: how many items of the last, partial round to cut in two, or null
+    int tail_cap, pairs;         // at most tail_cap; CTA pairs of the device
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
@@ -206,6 +208,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     }
     if (tid == 0) {
         *p.item_count = total_items;
+        if (p.tail_k) {
+            const int rem = p.pairs > 0 ? total_items % p.pairs : 0;
+            *p.tail_k = (rem > 0 && 2 * rem <= p.pairs) ? min(rem, p.tail_cap) : 0;
+        }
         if (p.item_off[p.batch] > p.max_items) atomicOr(p.status, kStatusBadTree);
     }
 }

@@ -109,8 +109,10 @@ struct VerifyParams {
     float* part_lse;            // [num_splits, total_q * 64]
     int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
     int split_share;            // two splits: the first one's share of a work item's tiles, in 1/1024 (0 = halves)
-    // one split, but the last tail_split work items cut in two (tail_share for the first part) and merged
-    int tail_split, tail_share;
+    // one split, but the last *tail_k (<= tail_cap) work items cut in two (tail_share for the first
+    // part) and merged; their partials are compact: tail_cap row tiles per split
+    int tail_cap, tail_share;
+    const int32_t* tail_k;      // written by the prep kernel, or null
     float scale_log2;           // softmax scale * log2(e)
     uint64_t timeout_ns;
     // sparse variant only
@@ -189,19 +191,21 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // ---- work unit: (work item, split of it, splits of it) ----
-    // Regular: one unit per (item, blockIdx.y).  With tail_split = k > 0 the
-    // whole items come first, then the first parts of the last k items, then
-    // their second parts.
+    // Regular: one unit per (item, blockIdx.y).  With k = *tail_k > 0 the whole
+    // items come first, then the first parts of the last k items, then their
+    // second parts; tail_j numbers a cut item among the k.
     grid_dependency_wait();     // the prep (and slot check) kernels' work list and metadata
     grid_launch_dependents();
     const int n_items = __ldg(p.item_count);
     int item_slot = blockIdx.x >> 1, split = blockIdx.y, nsplit = p.num_splits, share = p.split_share;
-    if (p.tail_split > 0) {
-        const int k = min(p.tail_split, n_items), whole = n_items - k;
-        if (item_slot >= whole) {
+    int tail_j = -1;
+    if (p.tail_k != nullptr) {
+        const int k = min(min(__ldg(p.tail_k), p.tail_cap), n_items), whole = n_items - k;
+        if (k > 0 && item_slot >= whole) {
             const int j = item_slot - whole;
             if (j >= 2 * k) return;
-            item_slot = whole + j % k;
+            tail_j = j % k;
+            item_slot = whole + tail_j;
             split = j / k;
             nsplit = 2;
             share = p.tail_share;
@@ -253,9 +257,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // lines.  own(part, v) fills v[32] with this unit's normalised columns
     // 32 part .. 32 part + 31 of the thread's row; lse_own is its lse.
     const long long out_rows = static_cast<long long>(p.total_q) * kHeads;
+    // rows of this tile in the partial buffers: its global rows, or the cut item's compact slot
+    const long long part_row0 = tail_j >= 0 ? static_cast<long long>(tail_j) * kRows : static_cast<long long>(qbase) * kHeads;
+    const long long part_rows = tail_j >= 0 ? static_cast<long long>(p.tail_cap) * kRows : out_rows;
     auto two_split_merge = [&](auto&& own, float lse_own) {
         int32_t* cnt = p.merge_cnt + (item_slot * 2 + static_cast<int>(c)) * 2;
-        float* lse2 = p.part_lse + static_cast<long long>(c) * 2 * out_rows;   // [half][split][row]
+        float* lse2 = p.part_lse + static_cast<long long>(c) * 2 * part_rows;   // [half][split][row]
+        const long long prow = part_row0 + r, pwrow = part_row0 + q4 * 32;   // this row / the warp's first
         const uint32_t ebuf = smem_u32(smem + kOffP) + q4 * 4096;
         const long long wrow = grow - lane;   // the warp's first row
         named_bar_sync(4, kSoftmaxThreads);
@@ -263,7 +271,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         named_bar_sync(4, kSoftmaxThreads);
         const int role = *reinterpret_cast<volatile int*>(&ctl->merge_role);
         if (role == 0) {
-            float* wdst = p.part_out + (static_cast<long long>(split) * out_rows + wrow) * kDLatent + kDLatentHalf * c;
+            float* wdst = p.part_out + (static_cast<long long>(split) * part_rows + pwrow) * kDLatent + kDLatentHalf * c;
             for (int part = 0; part < kDLatentHalf / 32; ++part) {
                 float v[32];
                 own(part, v);
@@ -282,7 +290,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 }
                 __syncwarp();
             }
-            if (row_valid) lse2[split * out_rows + grow] = lse_own;
+            if (row_valid) lse2[split * part_rows + prow] = lse_own;
             __threadfence();
             named_bar_sync(4, kSoftmaxThreads);
             if (r == 0) atomicExch(cnt + 1, 1);
@@ -305,7 +313,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t obuf = smem_u32(smem + kOffStages) + q4 * (32 * 1024);
         if (row_valid) {
             const float* wsrc =
-                p.part_out + (static_cast<long long>(other) * out_rows + wrow) * kDLatent + kDLatentHalf * c;
+                p.part_out + (static_cast<long long>(other) * part_rows + pwrow) * kDLatent + kDLatentHalf * c;
 #pragma unroll 4
             for (int i = 0; i < 32; ++i) {
 #pragma unroll
@@ -318,7 +326,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             cp_async_wait<0>();
         }
         __syncwarp();
-        const float lse_oth = row_valid ? lse2[other * out_rows + grow] : -INFINITY;
+        const float lse_oth = row_valid ? lse2[other * part_rows + prow] : -INFINITY;
         const float l0 = split == 0 ? lse_own : lse_oth, l1 = split == 0 ? lse_oth : lse_own;
         const float m = fmaxf(l0, l1);
         float lse_tot = -INFINITY, w0 = 0.f, w1 = 0.f;

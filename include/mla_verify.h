@@ -81,6 +81,10 @@ int mla_init(int device);
  * (clamped to [1, MLA_MAX_SPLITS]); 0 picks one from the shape: enough
  * (request, row-tile, split) work units to fill every SM of the current
  * device in whole waves, with at least 16 KV tiles of 64 keys per split.
+ * When 0 resolves to one split and a request has at least 12 KV tiles, the
+ * verify call may also cut the work items of its last, partial round of CTA
+ * pairs in two and merge them in the kernel (decided on the device from the
+ * exact item count); an explicit request of 1 never does.
  * Returns the count, or a negative mla_status on invalid arguments.
  */
 int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
@@ -88,7 +92,9 @@ int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
 
 /*
  * Bytes of device workspace mla_verify_attn needs for these sizes (with
- * `num_splits` resolved as by mla_verify_num_splits).  0 on invalid input.
+ * `num_splits` resolved as by mla_verify_num_splits, including room for the
+ * cut described there when `num_splits` is 0).  Pass the same `num_splits`
+ * to mla_verify_attn.  0 on invalid input.
  */
 size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_seq_len,
                                  int num_heads, int num_splits);

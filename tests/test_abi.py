@@ -178,3 +178,21 @@ def test_graph_create_needs_init_and_launch_checks(lib):
                                        2, 2, 0, 256, 1 << 20, None, None) == binding.MLA_ERR_INVALID_ARG
     assert binding.verify_graph_launch(None, 1, None) == binding.MLA_ERR_INVALID_ARG
     assert binding.verify_graph_destroy(None) == binding.MLA_OK
+
+
+def test_tail_cut_workspace_only_for_automatic_single_split(lib):
+    """With num_splits = 0 resolving to one split and items of >= 12 KV tiles,
+    the workspace holds room for cutting the last round's items (compact
+    partials of up to half the CTA pairs' row tiles); an explicit single split,
+    or short items, do not."""
+    # 4 requests, 24 KV tiles each: one split
+    assert binding.num_splits(4, 60, 32, 1516) == 1
+    auto = binding.workspace_size(4, 60, 32, 1516, splits=0)
+    one = binding.workspace_size(4, 60, 32, 1516, splits=1)
+    pairs = 152 // 2                      # no device here: the library assumes 152 SMs
+    assert auto - one >= (pairs // 2) * 128 * 512 * 4 * 2
+    # 1 request of 5 KV tiles: too short to cut
+    assert binding.workspace_size(1, 8, 8, 264, splits=0) == binding.workspace_size(1, 8, 8, 264, splits=1)
+    # the sparse variant (17 tiles at top-k 512) follows the same rule
+    assert binding.sparse_workspace_size(16, 512, 32, 512, splits=0) > binding.sparse_workspace_size(16, 512, 32, 512,
+                                                                                                    splits=1)

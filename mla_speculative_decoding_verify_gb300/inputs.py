@@ -5,19 +5,21 @@ shapes draft trees and lays the latent KV cache out in pages.  It holds none
 of the attention arithmetic, so the CUDA path and the fp64 oracle can both
 consume what it produces without sharing any of the method's code.
 
-Workloads follow the configurations of the verify-attention task (page
-"The Shared Memory Ceiling", sections "The Broader Context" and "Technical
-Deep Dive": 64 heads, a 512-dim latent c_kv plus a 64-dim k_rope per KV row,
+Five verify-attention workloads, shaped as the verify-kernel page describes
+the problem (page "The Shared Memory Ceiling", sections "The Broader Context"
+and "Technical Deep Dive": 64 heads, a 512-dim latent c_kv plus a 64-dim k_rope per KV row,
 a draft tree of query tokens per request, prefixes up to 65,536 tokens).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * values are N(0,1) drawn as float32 from numpy's PCG64 (ziggurat), then
     rounded to bf16 with round-to-nearest-even;
   * the tree tokens' own latents sit in the same paged cache right after the
     prefix, so ``seq_lens = prefix + n_tree``;
   * ``tree_parent`` holds request-local parents, -1 for a root, parent < i;
-  * outlier rows (config 2) scale the 512 c_kv dims by 8, not k_rope;
-  * shared-prefix groups (config 5) of 8 requests share the physical pages
+  * outlier rows (the 4 x 4096-token workload) scale the 512 c_kv dims by 8,
+    not k_rope;
+  * shared-prefix groups (the 64-request ragged workload) of 8 requests share
+    the physical pages
     of their first floor(min_prefix / page) pages, with identical content;
   * unused cache rows (tail of a last page, unreferenced pages) and unused
     block-table slots are poisoned (NaN rows, -1 slots) so a read out of

@@ -95,7 +95,7 @@ def test_outlier_rows_keep_tolerance():
     ref_o, ref_l = oracle.verify(inp)
     out, lse, status = run_gpu(inp)
     assert status == 0
-    assert_close(out, lse, ref_o, ref_l, "config 2 full")
+    assert_close(out, lse, ref_o, ref_l, "4 x 4096 outliers, full")
 
 
 _FULL = {}

@@ -72,7 +72,10 @@ const char *mla_error_string(int status);
  * Per-device set-up: checks that `device` is an sm_103 GPU, raises the
  * kernels' dynamic shared-memory limit and resolves the driver's tensor-map
  * encoder.  Call once per device, outside stream capture, before the first
- * verify call on that device.  Makes `device` current.  Idempotent.
+ * verify call on that device.  Makes `device` current.  Idempotent.  After
+ * cudaDeviceReset the device has a new context: call mla_init again before the
+ * next call on it (it sets the kernels up again and forgets cached device
+ * addresses of the old context).
  */
 int mla_init(int device);
 
@@ -150,7 +153,15 @@ int mla_verify_attn(const void *q_lat, const void *q_rope, const void *kv_cache,
                     void *workspace, size_t workspace_bytes);
 
 /*
- * Log-sum-exp merge of split-KV partials (flash-decoding combine).
+ * Log-sum-exp merge of split-KV partials (flash-decoding combine).  A long
+ * prefix with few requests is divided along the KV axis into splits, each
+ * attended separately (the decode kernel of page "The SMEM Ceiling", section
+ * "The Problem Space", is such a split kernel); their results are merged by
+ * the rescale-and-add step of the online softmax (page "The Shared Memory
+ * Ceiling", section "Technical Deep Dive": the softmax of the whole set is
+ * reached incrementally, earlier partial sums rescaled by the change of the
+ * running maximum), applied once per split with each split's log-sum-exp in
+ * place of its running maximum and normaliser.
  *
  *  part_out  device fp32 [num_splits, rows, 512]  each split's normalised output
  *  part_lse  device fp32 [num_splits, rows]       each split's natural-log LSE;
@@ -213,8 +224,9 @@ int mla_verify_sparse_attn(const void *q_lat, const void *q_rope, const void *kv
  *    overwrite the rest before reading it, so a call never sees an earlier
  *    call's data, but calls whose work overlaps on the GPU (other streams,
  *    other host threads) race on it and must be serialised by the caller.
- *  - The device status word is not readable for this variant; rows of a
- *    request with invalid data are still written as out = 0, lse = -inf.
+ *  - The device status word (as for mla_verify_attn) lives in the array; read
+ *    it with mla_verify_noalloc_read_status once the call's stream has been
+ *    synchronised and before the next call on the device.
  */
 int mla_verify_attn_noalloc(const void *q_lat, const void *q_rope, const void *kv_cache,
                             const int32_t *block_table, const int32_t *seq_lens,
@@ -222,6 +234,15 @@ int mla_verify_attn_noalloc(const void *q_lat, const void *q_rope, const void *k
                             float *out, float *lse, cudaStream_t stream,
                             int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
                             int page_size, int num_pages, int max_pages_per_seq);
+
+/*
+ * Copies the device status word of the last mla_verify_attn_noalloc call on the
+ * current device (the bits of mla_read_status) to *device_status.  Synchronous
+ * (a device-to-host copy); call it after synchronising the verify call's
+ * stream.  No counterpart in the page text either.  MLA_ERR_INVALID_ARG for a
+ * NULL pointer, MLA_ERR_CUDA if the copy fails.
+ */
+int mla_verify_noalloc_read_status(int *device_status);
 
 /*
  * Paged-cache steps around verification ("The Shared Memory Ceiling", section
@@ -237,10 +258,12 @@ int mla_verify_attn_noalloc(const void *q_lat, const void *q_rope, const void *k
  *
  * mla_tree_kv_append: writes tree_kv (device bf16 [total_q, 576], tokens back
  * to back in request order, as in q_lat) into each request's tree region of
- * kv_cache ([num_pages, page_size, 576], 16-byte aligned).  A request whose
- * n_tree is outside [0, 64] or above its seq_len sets status bit
- * 1 << MLA_ERR_BAD_TREE; one whose tree region maps to a block id outside
- * [0, num_pages) sets 1 << MLA_ERR_BAD_BLOCK; either request is left untouched.
+ * kv_cache ([num_pages, page_size, 576], 16-byte aligned).  Request b's rows
+ * start at the sum of n_tree[0..b), a negative count taken as 0.  A request
+ * whose n_tree is outside [0, 64] or above its seq_len, or whose rows would
+ * reach past total_q, sets status bit 1 << MLA_ERR_BAD_TREE; one whose tree
+ * region maps to a block id outside [0, num_pages) sets 1 << MLA_ERR_BAD_BLOCK;
+ * either request is left untouched (no row outside [0, total_q) is read).
  *
  * mla_tree_kv_accept: after verification, accept_len[b] (device int32 [batch])
  * tokens of request b are accepted; accept_idx (device int32 [total_q], same

@@ -36,6 +36,7 @@ MAX_TOPK = 2048
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
             "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc",
+            "mla_verify_noalloc_read_status",
             "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept",
             "mla_verify_sparse_num_splits", "mla_verify_sparse_workspace_size", "mla_verify_sparse_attn",
             "mla_verify_graph_create", "mla_verify_graph_launch", "mla_verify_graph_destroy")
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.mla_verify_attn_noalloc.restype = i32
         L.mla_verify_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                               i32, i32, i32, i32, i32, i32, i32, i32]
+        L.mla_verify_noalloc_read_status.restype = i32
+        L.mla_verify_noalloc_read_status.argtypes = [vp]
         L.mla_split_combine.restype = i32
         L.mla_split_combine.argtypes = [vp, vp, i32, i32, vp, vp, vp]
         L.mla_set_profile_events.restype = i32
@@ -145,6 +148,14 @@ def verify_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_t
                                      n_tree, float(scale), out, lse, stream, batch, total_q,
                                      max_tree, max_seq_len, num_heads, page_size, num_pages,
                                      max_pages_per_seq, num_splits, workspace, workspace_bytes))
+
+
+def noalloc_read_status() -> int:
+    """Device status word of the last allocation-free call on the current device
+    (synchronous copy; synchronise the call's stream first)."""
+    v = ctypes.c_int(0)
+    check(lib().mla_verify_noalloc_read_status(ctypes.byref(v)), "mla_verify_noalloc_read_status")
+    return int(v.value)
 
 
 def verify_attn_noalloc(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree,

@@ -28,18 +28,19 @@ struct KvOpParams {
     const int32_t* accept_idx;   // accept: [total_q] path node indices, accept_len[b] of them per request
     int32_t* new_seq_lens;       // accept: [batch]
     int* status;                 // [1], zeroed by the host before the launch
-    int batch, page_size, max_pages, num_pages;
+    int batch, total_q, page_size, max_pages, num_pages;
 };
 
-// Sum of n_tree[0..b) over the block: the first tree token of request b.
-__device__ __forceinline__ int request_offset(const int32_t* n_tree, int b) {
-    __shared__ int partial[kKvOpThreads / 32];
-    int v = 0;
-    for (int i = threadIdx.x; i < b; i += blockDim.x) v += __ldg(n_tree + i);
+// Sum of n_tree[0..b) over the block, a negative count read as 0: the first
+// tree token of request b (64-bit, so that no sum of counts wraps).
+__device__ __forceinline__ long long request_offset(const int32_t* n_tree, int b) {
+    __shared__ long long partial[kKvOpThreads / 32];
+    long long v = 0;
+    for (int i = threadIdx.x; i < b; i += blockDim.x) v += max(__ldg(n_tree + i), 0);
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if ((threadIdx.x & 31) == 0) partial[threadIdx.x >> 5] = v;
     __syncthreads();
-    int s = 0;
+    long long s = 0;
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += partial[w];
     __syncthreads();
     return s;
@@ -70,7 +71,11 @@ __global__ void __launch_bounds__(kKvOpThreads, 1) mla_tree_append_kernel(const 
         return;
     }
     const int P = L - T;
-    const int off = request_offset(p.n_tree, b);
+    const long long off = request_offset(p.n_tree, b);
+    if (off + T > p.total_q) {   // the request's rows of tree_kv lie past the end: malformed lengths
+        if (threadIdx.x == 0) atomicOr(p.status, kKvStatusBadTree);
+        return;
+    }
     if (!tree_pages_ok(p, b, P, T)) {
         if (threadIdx.x == 0) atomicOr(p.status, kKvStatusBadBlock);
         return;
@@ -96,7 +101,15 @@ __global__ void __launch_bounds__(kKvOpThreads, 1) mla_tree_accept_kernel(const 
         return;
     }
     const int P = L - T;
-    const int off = request_offset(p.n_tree, b);
+    const long long off = request_offset(p.n_tree, b);
+    // the request's rows of tree_parent / accept_idx lie inside [0, total_q)
+    if (off + T > p.total_q) {
+        if (threadIdx.x == 0) {
+            atomicOr(p.status, kKvStatusBadTree);
+            p.new_seq_lens[b] = L;
+        }
+        return;
+    }
     // the tree (parents earlier than their children) and the path (a chain from a root)
     bool bad = A < 0 || A > T;
     for (int i = threadIdx.x; i < T; i += blockDim.x) {

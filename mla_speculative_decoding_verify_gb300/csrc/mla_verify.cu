@@ -22,6 +22,10 @@
 #include "prep_kernel.cuh"
 #include "verify_kernel.cuh"
 
+namespace mla_internal {
+void noalloc_forget_device(int dev);   // mla_verify_noalloc.cu
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -307,7 +311,9 @@ int mla_init(int device) {
     if (device < 0 || device >= kMaxDevices) return MLA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
-    if (g_dev[device].ready) return MLA_OK;
+    // Every call sets the device up again (cheap): after cudaDeviceReset the
+    // device has a new context, without the kernels' attributes of the old one.
+    mla_internal::noalloc_forget_device(device);
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MLA_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return MLA_ERR_UNSUPPORTED;  // built for sm_103a only
@@ -568,6 +574,7 @@ static int kv_op_setup(void* kv_cache, const int32_t* block_table, const int32_t
     kp->n_tree = n_tree;
     kp->status = static_cast<int*>(workspace);
     kp->batch = batch;
+    kp->total_q = total_q;
     kp->page_size = page_size;
     kp->max_pages = max_pages_per_seq;
     kp->num_pages = num_pages;

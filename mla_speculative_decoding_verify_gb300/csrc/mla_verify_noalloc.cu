@@ -47,6 +47,23 @@ int scratch_address(void** out) {
 
 }  // namespace
 
+namespace mla_internal {
+// Called by mla_init: drop the cached address of the scratch on `dev` (a reset
+// device has a new context, in which the address is looked up again).
+__attribute__((visibility("hidden"))) void noalloc_forget_device(int dev) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    g_noalloc_ptr[dev] = nullptr;
+}
+}  // namespace mla_internal
+
+extern "C" int mla_verify_noalloc_read_status(int* device_status) {
+    if (!device_status) return MLA_ERR_INVALID_ARG;
+    // the status word is the first word of the scratch (the workspace layout's first field)
+    if (cudaMemcpyFromSymbol(device_status, g_noalloc_scratch, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
 extern "C" int mla_verify_attn_noalloc(const void* q_lat, const void* q_rope, const void* kv_cache,
                                        const int32_t* block_table, const int32_t* seq_lens,
                                        const int32_t* tree_parent, const int32_t* n_tree, float scale,

@@ -21,7 +21,12 @@ implemented here:
 
 Both leave a request untouched and report it in the status bits when its tree
 or path is malformed (bit 1 << 6) or a block id it touches is out of range
-(bit 1 << 7).  Rows are moved as raw 16-bit patterns: the results are exact.
+(bit 1 << 7).  A request's rows of the per-token arrays (tree_kv, tree_parent,
+accept_idx, all [total_q, ...]) start at the sum of the earlier counts, a
+negative count taken as 0; a request whose rows would reach past total_q is
+malformed too (a reading: the pages define no error contract, and this one
+never reads outside the arrays).  Rows are moved as raw 16-bit patterns: the
+results are exact.
 """
 from __future__ import annotations
 
@@ -34,7 +39,9 @@ STATUS_BAD_BLOCK = 1 << 7
 
 
 def _offsets(n_tree):
-    n_tree = np.asarray(n_tree, dtype=np.int64)
+    """First tree token of each request: the running sum of the counts, a negative
+    count taken as 0 (such a request is itself rejected as malformed)."""
+    n_tree = np.maximum(np.asarray(n_tree, dtype=np.int64), 0)
     return np.concatenate([[0], np.cumsum(n_tree)]).astype(np.int64)
 
 
@@ -59,11 +66,12 @@ def tree_kv_append(kv_cache, block_table, seq_lens, n_tree, tree_kv, page_size):
     num_pages = cache.shape[0]
     flat = cache.reshape(num_pages * page_size, D_KV)
     tree_kv = np.asarray(tree_kv, dtype=np.uint16).reshape(-1, D_KV)
+    total_q = tree_kv.shape[0]
     off = _offsets(n_tree)
     status = 0
     for b in range(len(seq_lens)):
         T, L = int(n_tree[b]), int(seq_lens[b])
-        if T < 0 or T > MAX_TREE or T > L:
+        if T < 0 or T > MAX_TREE or T > L or off[b] + T > total_q:
             status |= STATUS_BAD_TREE
             continue
         P = L - T
@@ -82,11 +90,12 @@ def tree_kv_accept(kv_cache, block_table, seq_lens, n_tree, tree_parent, accept_
     num_pages = cache.shape[0]
     flat = cache.reshape(num_pages * page_size, D_KV)
     off = _offsets(n_tree)
+    total_q = len(tree_parent)
     new_lens = np.array(seq_lens, dtype=np.int32, copy=True)
     status = 0
     for b in range(len(seq_lens)):
         T, L, A = int(n_tree[b]), int(seq_lens[b]), int(accept_len[b])
-        if T < 0 or T > MAX_TREE or T > L:
+        if T < 0 or T > MAX_TREE or T > L or off[b] + T > total_q:
             status |= STATUS_BAD_TREE
             continue
         P = L - T

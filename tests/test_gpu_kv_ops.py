@@ -138,6 +138,30 @@ def test_malformed_paths_and_bad_blocks_leave_requests_untouched():
     np.testing.assert_array_equal(got, ref)
 
 
+def test_tree_counts_outside_total_q_are_rejected_without_stray_reads():
+    """A negative tree count and counts that run past total_q: the GPU flags the
+    malformed request, leaves it untouched and reads no row outside the arrays;
+    the other requests match the oracle bit for bit."""
+    for prefixes, trees, fix in (((70, 40, 100), (2, 3, 8), {0: -5}), ((70, 40), (5, 3), {1: 13})):
+        inp = I.make_inputs(list(prefixes), list(trees), tree_kind="uniform", seed=15, stream=915)
+        for b, v in fix.items():
+            inp.n_tree[b] = v
+        rows = rand_rows(inp.total_q, 16)
+        ref, ref_st = K.tree_kv_append(inp.kv_cache, inp.block_table, inp.seq_lens, inp.n_tree, rows,
+                                       inp.page_size)
+        got, st, _ = gpu_append(inp, rows)
+        assert st == ref_st and st & K.STATUS_BAD_TREE
+        np.testing.assert_array_equal(got, ref)
+        acc_len = np.ones(inp.batch, np.int32)
+        acc_idx = np.zeros(inp.total_q, np.int32)
+        ref2, ref_lens, ref_st2 = K.tree_kv_accept(inp.kv_cache, inp.block_table, inp.seq_lens, inp.n_tree,
+                                                   inp.tree_parent, acc_len, acc_idx, inp.page_size)
+        got2, lens, st2 = gpu_accept(inp, acc_len, acc_idx)
+        assert st2 == ref_st2 and st2 & K.STATUS_BAD_TREE
+        np.testing.assert_array_equal(lens, ref_lens)
+        np.testing.assert_array_equal(got2, ref2)
+
+
 @pytest.mark.parametrize("cfg", [3, 5])
 def test_full_size_append_then_accept(cfg):
     """Workload-sized caches (302 MB for c3; c5 with shared prefix pages), compared whole."""

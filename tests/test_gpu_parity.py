@@ -163,12 +163,16 @@ def test_invalid_tree_reported_and_rows_zeroed():
 
 
 def test_bad_block_id_reported():
-    inp = I.make_inputs([200], [3], tree_kind="uniform", seed=4, stream=504)
+    """A block id outside the cache: status bit, the request's rows written as
+    out = 0, lse = -inf (the header's contract), its neighbour unaffected."""
+    inp = I.make_inputs([200, 130], [3, 4], tree_kind="uniform", seed=4, stream=504)
+    ref_o, ref_l = oracle.verify(inp)          # on the intact block table
     inp.block_table = inp.block_table.copy()
     inp.block_table[0, 1] = inp.num_pages + 5
     out, lse, status = run_gpu(inp)
     assert status & (1 << binding.MLA_ERR_BAD_BLOCK)
-    assert np.isfinite(out).all()
+    assert not out[:3].any() and np.isneginf(lse[:3]).all()
+    assert_close(out[3:], lse[3:], ref_o[3:], ref_l[3:], "valid request next to a bad block id")
 
 
 def test_argument_errors_before_launch():

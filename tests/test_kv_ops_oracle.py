@@ -189,3 +189,36 @@ def test_shared_prefix_pages_are_not_touched():
     shared = set(int(p) for p in inp.block_table[0, :200 // inp.page_size])
     for p in shared:
         np.testing.assert_array_equal(cache[p].view(np.uint16), inp.kv_cache[p].view(np.uint16))
+
+
+def test_request_rows_follow_clamped_counts_and_stay_inside_total_q():
+    """A negative tree count takes no rows (later requests start where it would have),
+    and a request whose rows would reach past total_q is rejected untouched."""
+    # negative count: request 0 is malformed; requests 1 and 2 read rows 0..2 and 3..10
+    inp = small_inputs(11, prefixes=(70, 40, 100), trees=(2, 3, 8))
+    n_tree = inp.n_tree.copy()
+    n_tree[0] = -5
+    rows = random_rows(inp.total_q, 12)
+    got, st = K.tree_kv_append(inp.kv_cache, inp.block_table, inp.seq_lens, n_tree, rows, inp.page_size)
+    assert st == K.STATUS_BAD_TREE
+    np.testing.assert_array_equal(logical_rows(got, inp, 0, int(inp.seq_lens[0])),
+                                  logical_rows(inp.kv_cache, inp, 0, int(inp.seq_lens[0])))
+    for b, lo in ((1, 0), (2, 3)):
+        T, L = int(n_tree[b]), int(inp.seq_lens[b])
+        np.testing.assert_array_equal(logical_rows(got, inp, b, L)[L - T:], rows[lo:lo + T])
+    # counts that reach past total_q: request 1 (rows 5 .. 17 of 8) is rejected, request 0 appended
+    inp = small_inputs(13, prefixes=(70, 40), trees=(5, 3))
+    n_tree = inp.n_tree.copy()
+    n_tree[1] = 13
+    rows = random_rows(inp.total_q, 14)
+    got, st = K.tree_kv_append(inp.kv_cache, inp.block_table, inp.seq_lens, n_tree, rows, inp.page_size)
+    assert st == K.STATUS_BAD_TREE
+    np.testing.assert_array_equal(logical_rows(got, inp, 0, 75)[70:], rows[:5])
+    np.testing.assert_array_equal(logical_rows(got, inp, 1, 43), logical_rows(inp.kv_cache, inp, 1, 43))
+    acc_len = np.array([1, 1], np.int32)
+    acc_idx = np.zeros(inp.total_q, np.int32)
+    got, lens, st = K.tree_kv_accept(inp.kv_cache, inp.block_table, inp.seq_lens, n_tree, inp.tree_parent,
+                                     acc_len, acc_idx, inp.page_size)
+    assert st & K.STATUS_BAD_TREE
+    assert int(lens[1]) == int(inp.seq_lens[1])
+    np.testing.assert_array_equal(logical_rows(got, inp, 1, 43), logical_rows(inp.kv_cache, inp, 1, 43))

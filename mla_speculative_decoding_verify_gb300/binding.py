@@ -13,7 +13,9 @@ from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_NAME = "libmla_verify.so"
-LIB_PATH = os.path.join(_HERE, LIB_NAME)
+# The in-tree build; MLA_VERIFY_LIBRARY names another build of the same library
+# (the tests use it to load the fault-injection build in a separate process).
+LIB_PATH = os.environ.get("MLA_VERIFY_LIBRARY") or os.path.join(_HERE, LIB_NAME)
 
 MLA_OK = 0
 MLA_ERR_INVALID_ARG = 1

@@ -43,5 +43,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return OUT
 
 
+OUT_FAULTS = os.path.join(_HERE, "libmla_verify_faults.so")
+
+
+def build_fault_injection(force: bool = False) -> str:
+    """The same library compiled with MLA_FAULT_INJECTION: 5 ms pipeline waits and
+    mla_debug_set_fault(kind), for the tests of the timeout paths.  Never the
+    library the package loads unless MLA_VERIFY_LIBRARY names it."""
+    if not force and os.path.exists(OUT_FAULTS) and all(
+            os.path.getmtime(f) <= os.path.getmtime(OUT_FAULTS) for f in [SRC, SRC_NOALLOC] + HEADERS):
+        return OUT_FAULTS
+    tmp = OUT_FAULTS + f".tmp{os.getpid()}"
+    cmd = [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-DMLA_FAULT_INJECTION", "-Xcompiler", "-fPIC",
+           "-shared", "-I", os.path.join(ROOT, "include"), SRC, SRC_NOALLOC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, OUT_FAULTS)
+    return OUT_FAULTS
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

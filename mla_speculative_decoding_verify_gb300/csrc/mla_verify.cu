@@ -29,7 +29,11 @@ void noalloc_forget_device(int dev);   // mla_verify_noalloc.cu
 namespace {
 
 constexpr int kMaxDevices = 64;
+#ifdef MLA_FAULT_INJECTION
+constexpr uint64_t kDefaultTimeoutNs = 5000000ull;      // test build: 5 ms per pipeline wait
+#else
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per pipeline wait
+#endif
 
 struct DeviceState {
     bool ready = false;
@@ -712,3 +716,11 @@ int mla_verify_graph_destroy(mla_verify_graph* graph) {
 
 }  // extern "C"
 
+
+#ifdef MLA_FAULT_INJECTION
+// Test build only (not part of the shipped library's interface): choose the
+// fault the verify kernel injects from now on (0 = none; see verify_kernel.cuh).
+extern "C" int mla_debug_set_fault(int kind) {
+    return cudaMemcpyToSymbol(mla::g_fault_kind, &kind, sizeof(int)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+#endif

@@ -137,6 +137,7 @@ struct Ctrl {
     uint64_t q_ready;
     uint64_t drain_qk;
     uint64_t drain_pv;
+    uint64_t never;        // fault injection: nothing arrives on it
     uint32_t tmem_base;
     int abort;
     int lo_flag[2];
@@ -147,6 +148,21 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 __device__ __forceinline__ void raise_status(int* status, int bit) { atomicOr(status, bit); }
+
+// Fault injection (a test build only, compiled with MLA_FAULT_INJECTION): make
+// one bounded wait run out so that the timeout paths can be tested without
+// faulting or hanging the GPU.  Kinds, all in the first work unit (item 0,
+// split 0) and CTA 0 of its pair:
+//   1  the QK issuer waits for KV tile 1 on a barrier that nothing completes;
+//   2  (two splits merged in the kernel) the first unit of the row tile never
+//      marks its partial written, so the second one's poll runs out;
+//   3  the softmax threads do not send the partial scores of tile 1.
+#ifdef MLA_FAULT_INJECTION
+__device__ int g_fault_kind;
+__device__ __forceinline__ int fault_kind() { return *reinterpret_cast<volatile int*>(&g_fault_kind); }
+#else
+__device__ __forceinline__ constexpr int fault_kind() { return 0; }
+#endif
 
 // Which KV tiles [t0, t1) split `s` of `S` covers, for a request of n tiles.  With
 // two splits and share > 0 the first split takes share / 1024 of the tiles.
@@ -293,7 +309,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (row_valid) lse2[split * part_rows + prow] = lse_own;
             __threadfence();
             named_bar_sync(4, kSoftmaxThreads);
-            if (r == 0) atomicExch(cnt + 1, 1);
+            const bool skip_mark = fault_kind() == 2 && item_slot == 0 && c == 0;
+            if (r == 0 && !skip_mark) atomicExch(cnt + 1, 1);
             return;
         }
         if (r == 0) {
@@ -461,6 +478,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         mbar_init(&ctl->q_ready, kSoftmaxThreads);
         mbar_init(&ctl->drain_qk, 1);
         mbar_init(&ctl->drain_pv, 1);
+        mbar_init(&ctl->never, 1);
         mbar_init(&ctl->stg_free, 1);
         ctl->abort = 0;
         // byte count of the first incoming partial, posted before the peer can send
@@ -642,8 +660,10 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             const int st = jj % kStages;
             const int x = jj & 1;
             const bool tail = !kSparse && (t0 + jj) * kBlockN + kBlockN > L;
-            ok = tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
-                      : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
+            const bool inject = fault_kind() == 1 && item_slot == 0 && split == 0 && c == 0 && jj == 1;
+            ok = inject ? mbar_wait(&ctl->never, 0, abort_flag, lim)
+                 : tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
+                        : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
             // S buffer x held tile jj - 2; the softmax threads have read it out
             if (ok && jj >= 2) ok = mbar_wait(&ctl->s_free[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
             ok = __all_sync(0xffffffffu, ok);
@@ -795,7 +815,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (r == 0 && ok) {
                 // the peer has read the partial this CTA sent before (its receive buffer is free)
                 if (t >= 1) ok = mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
-                if (ok) bulk_copy_to_peer(xbuf_peer, stg_local, kXBufBytes, xfull_peer);
+                const bool skip_send = fault_kind() == 3 && item_slot == 0 && split == 0 && c == 0 && t == 1;
+                if (ok && !skip_send) bulk_copy_to_peer(xbuf_peer, stg_local, kXBufBytes, xfull_peer);
             }
         };
 

@@ -53,6 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload measurements (c2, c4, c5, sparse)")
     ap.add_argument("--cpu-rows", type=int, default=12288, help="oracle rows timed for cpu_baseline (about 10 s)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
@@ -205,6 +206,90 @@ def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7, topk_idx=None)
     return {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{len(sample)} of {total_rows} output rows, fp64 C oracle, all host threads, "
                       f"{dt:.2f} s wall"}
+
+
+# ------------------------------------------------------------------ the other workloads
+
+# The metric covers prefixes of 4k to 64k: after the headline workload the
+# default run measures these too (kernel time only), so that one bench line
+# records every configuration: name -> (workload, KV splits (0 = library's
+# choice), top-k slots for the sparse variant or None).
+SWEEP = {"c2": ("c2", 0, None), "c4_16splits": ("c4", 16, None), "c5": ("c5", 0, None),
+         "c3_sparse_top512": ("c3", 0, 512)}
+
+
+def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dict:
+    """Kernel time, throughput, roofline fraction and profiled DRAM traffic of the
+    SWEEP workloads, timed like the headline one (CUDA events recorded by the
+    library around the fused kernel, L2 flushed between steps)."""
+    import torch
+
+    from mla_speculative_decoding_verify_gb300 import binding, inputs as I, metrics
+    dev = torch.device(f"cuda:{ranks.local}")
+    peaks, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    res = {}
+    for key, (wl, req, topk) in SWEEP.items():
+        inp = I.config_inputs(WORKLOADS[wl], seed=args.seed)
+        db = binding.DeviceBatch(inp, dev)
+        out = torch.empty((inp.total_q, inp.num_heads, 512), dtype=torch.float32, device=dev)
+        lse = torch.empty((inp.total_q, inp.num_heads), dtype=torch.float32, device=dev)
+        if topk:
+            tk = I.topk_indices(inp, topk, seed=args.seed + 3)
+            d_tk = torch.from_numpy(tk).to(dev)
+            splits = binding.sparse_num_splits(inp.batch, inp.total_q, inp.max_tree, topk, inp.num_heads, req)
+            ws = torch.empty(binding.sparse_workspace_size(inp.batch, inp.total_q, inp.max_tree, topk,
+                                                           inp.num_heads, req), dtype=torch.uint8, device=dev)
+            flops, kvb = metrics.sparse_flops(inp, tk), metrics.sparse_kv_bytes(inp, tk)
+
+            def step():
+                binding.verify_sparse(db, d_tk, req, out=out, lse=lse, workspace=ws, stream=stream)
+        else:
+            splits = binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads, req)
+            ws = torch.empty(binding.workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
+                                                    inp.num_heads, req), dtype=torch.uint8, device=dev)
+            flops, kvb = metrics.algorithmic_flops(inp), metrics.kv_bytes(inp)
+
+            def step():
+                binding.verify(db, req, out=out, lse=lse, workspace=ws, stream=stream)
+        for _ in range(warmup):
+            flush.zero_()
+            step()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in kev:
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            flush.zero_()
+            binding.set_profile_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+            sev[i][0].record(stream)
+            step()
+            sev[i][1].record(stream)
+        binding.set_profile_events(None, None)
+        torch.cuda.synchronize(dev)
+        status = binding.read_status(ws.data_ptr())
+        k_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
+        s_ms = sum(a.elapsed_time(b) for a, b in sev) / steps
+        units = int(((inp.n_tree + 1) // 2).sum() * splits)
+        traffic_key = f"{wl}/sparse-top{topk}" if topk else (f"{wl}/{splits}splits" if req else wl)
+        e = {"workload": inp.name, "num_splits": splits, "kernel_ms": k_ms, "step_ms": s_ms,
+             "tflops": flops / (k_ms * 1e-3) / 1e12, "kv_gbps": kvb / (k_ms * 1e-3) / 1e9,
+             "algorithmic_gflop": flops / 1e9, "device_status": status, "steps": steps,
+             "traffic": profiled_traffic(traffic_key, units)}
+        if topk:
+            e.update(topk=topk, bound="hbm", frac=e["kv_gbps"] / float(peaks["hbm_gbs"]),
+                     peak=float(peaks["hbm_gbs"]), unit="GB/s")
+        else:
+            e.update(bound="tensor", frac=e["tflops"] / float(peaks["bf16_tflops"]),
+                     peak=float(peaks["bf16_tflops"]), unit="TFLOP/s")
+        e["peak_source"] = f"{peak_kind}, MEASURED_PEAKS.json" if peak_kind == "measured" else "fallback"
+        res[key] = e
+        del db, out, lse, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------------------ our arm
@@ -474,6 +559,10 @@ def run_ours(args, ranks: Ranks):
         result["config"]["topk"] = args.topk
     if ranks.rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, flops, args.cpu_rows, topk_idx=topk_idx if sparse else None)
+    if not sparse and ranks.world == 1 and not args.no_sweep:
+        del db
+        torch.cuda.empty_cache()
+        result["per_workload"] = sweep_workloads(args, ranks)
     return result
 
 

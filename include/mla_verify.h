@@ -175,6 +175,33 @@ int mla_split_combine(const float *part_out, const float *part_lse, int num_spli
                       float *out, float *lse, cudaStream_t stream);
 
 /*
+ * Splits split_begin .. split_begin + split_count - 1 of num_splits of every
+ * request's KV, each one's normalised partial and log-sum-exp written to
+ * part_out (device fp32 [split_count, total_q * 64, 512]) and part_lse (device
+ * fp32 [split_count, total_q * 64]); nothing else is written.  Split s covers
+ * KV tiles (64 keys) [n*s/S, n*(s+1)/S) of a request of n tiles (integer
+ * division), so the tree's own keys fall in the last split.  For sharding one
+ * long request's prefix across GPUs (the pages' serving setup runs on eight
+ * cards: page "The 99KB Barrier", sections "Message Snapshot" and "The
+ * Investigation Leading Up to This Message"): GPU r holds the KV pages
+ * of its splits only -- the block table must still name a valid page for
+ * every position, but pages outside the computed splits are never read --
+ * computes its splits, the GPUs exchange the partials once (all-gather), and
+ * mla_split_combine merges them.  Other arguments as for mla_verify_attn; the
+ * workspace is sized by mla_verify_workspace_size(..., num_splits = 1).  No
+ * sparse form.  Returns MLA_ERR_INVALID_ARG for an empty or out-of-range split
+ * range.
+ */
+int mla_verify_attn_split_range(const void *q_lat, const void *q_rope, const void *kv_cache,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                const int32_t *tree_parent, const int32_t *n_tree, float scale,
+                                float *part_out, float *part_lse, cudaStream_t stream,
+                                int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
+                                int page_size, int num_pages, int max_pages_per_seq, int num_splits,
+                                int split_begin, int split_count, void *workspace,
+                                size_t workspace_bytes);
+
+/*
  * Sparse (top-k) tree verification ("The SMEM Ceiling", section "The Problem
  * Space": during decode each token attends to a sparse set of previous tokens
  * chosen by a top-k index selection).  Arguments as for mla_verify_attn, plus

@@ -38,7 +38,7 @@ MAX_TOPK = 2048
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
             "mla_verify_workspace_size", "mla_verify_attn", "mla_split_combine",
             "mla_read_status", "mla_set_profile_events", "mla_verify_attn_noalloc",
-            "mla_verify_noalloc_read_status",
+            "mla_verify_noalloc_read_status", "mla_verify_attn_split_range",
             "mla_tree_kv_workspace_size", "mla_tree_kv_append", "mla_tree_kv_accept",
             "mla_verify_sparse_num_splits", "mla_verify_sparse_workspace_size", "mla_verify_sparse_attn",
             "mla_verify_graph_create", "mla_verify_graph_launch", "mla_verify_graph_destroy")
@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
         L.mla_verify_attn_noalloc.restype = i32
         L.mla_verify_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                               i32, i32, i32, i32, i32, i32, i32, i32]
+        L.mla_verify_attn_split_range.restype = i32
+        L.mla_verify_attn_split_range.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz]
         L.mla_verify_noalloc_read_status.restype = i32
         L.mla_verify_noalloc_read_status.argtypes = [vp]
         L.mla_split_combine.restype = i32
@@ -150,6 +153,18 @@ def verify_attn(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_t
                                      n_tree, float(scale), out, lse, stream, batch, total_q,
                                      max_tree, max_seq_len, num_heads, page_size, num_pages,
                                      max_pages_per_seq, num_splits, workspace, workspace_bytes))
+
+
+def verify_attn_split_range(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale,
+                            part_out, part_lse, stream, batch, total_q, max_tree, max_seq_len, num_heads,
+                            page_size, num_pages, max_pages_per_seq, num_splits, split_begin, split_count,
+                            workspace, workspace_bytes) -> int:
+    """Raw call: the partials of splits split_begin .. + split_count - 1 of num_splits; returns the status."""
+    return int(lib().mla_verify_attn_split_range(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent,
+                                                 n_tree, float(scale), part_out, part_lse, stream, batch, total_q,
+                                                 max_tree, max_seq_len, num_heads, page_size, num_pages,
+                                                 max_pages_per_seq, num_splits, split_begin, split_count,
+                                                 workspace, workspace_bytes))
 
 
 def noalloc_read_status() -> int:
@@ -276,6 +291,32 @@ def verify(db: "DeviceBatch", num_splits_req: int = 0, out=None, lse=None, works
                        workspace.data_ptr(), workspace.numel())
     check(code, "mla_verify_attn")
     return out, lse, workspace
+
+
+def verify_split_range(db: "DeviceBatch", num_splits: int, split_begin: int, split_count: int,
+                       part_out=None, part_lse=None, workspace=None, stream=None):
+    """Partials of a range of KV splits on a DeviceBatch: returns (part_out
+    [split_count, total_q, 64, 512], part_lse [split_count, total_q, 64], workspace)."""
+    import torch
+    inp = db.inp
+    if part_out is None:
+        part_out = torch.empty((split_count, inp.total_q, inp.num_heads, D_LATENT), dtype=torch.float32,
+                               device=db.device)
+    if part_lse is None:
+        part_lse = torch.empty((split_count, inp.total_q, inp.num_heads), dtype=torch.float32, device=db.device)
+    need = workspace_size(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len, inp.num_heads, 1)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=db.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(db.device)
+    check(verify_attn_split_range(db.q_lat.data_ptr(), db.q_rope.data_ptr(), db.kv_cache.data_ptr(),
+                                  db.block_table.data_ptr(), db.seq_lens.data_ptr(), db.tree_parent.data_ptr(),
+                                  db.n_tree.data_ptr(), inp.scale, part_out.data_ptr(), part_lse.data_ptr(),
+                                  stream.cuda_stream, inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len,
+                                  inp.num_heads, inp.page_size, inp.num_pages, inp.max_pages_per_seq, num_splits,
+                                  split_begin, split_count, workspace.data_ptr(), workspace.numel()),
+          "mla_verify_attn_split_range")
+    return part_out, part_lse, workspace
 
 
 def append_tree(db: "DeviceBatch", tree_kv, workspace=None, stream=None):

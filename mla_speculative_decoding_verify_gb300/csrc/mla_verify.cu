@@ -366,7 +366,12 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
                        float* out, float* lse, cudaStream_t stream, int batch, int total_q, int max_tree,
                        int max_seq_len, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
                        int num_splits, void* workspace, size_t workspace_bytes, const int32_t* topk_idx,
-                       int topk, bool graph_capture = false) {
+                       int topk, bool graph_capture = false, int split_begin = 0, int split_count = 0) {
+    // split_count > 0: compute only splits split_begin .. split_begin + split_count - 1 of
+    // num_splits, each one's partial into out / lse viewed as [split_count, rows, 512] / [split_count, rows]
+    const bool range = split_count > 0;
+    if (range && (topk > 0 || num_splits < 1 || split_begin < 0 || split_begin + split_count > num_splits))
+        return num_splits > MLA_MAX_SPLITS ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
     // ---- host-checkable arguments ----
     if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
         num_splits < 0 || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
@@ -387,8 +392,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
                                 : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
     if (splits <= 0) return MLA_ERR_INVALID_ARG;
     const int item_tiles = topk > 0 ? sparse_tiles(topk) : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
-    const TailPlan tail = launch_tail_plan(topk > 0, item_tiles, num_splits, splits);
-    const Layout lay = make_layout(batch, total_q, splits, topk > 0, tail.cap);
+    const TailPlan tail = range ? TailPlan{} : launch_tail_plan(topk > 0, item_tiles, num_splits, splits);
+    // a range of splits writes its partials to the caller's buffers: no partials in the workspace
+    const Layout lay = make_layout(batch, total_q, range ? 1 : splits, topk > 0, tail.cap);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_WORKSPACE;
 
@@ -399,8 +405,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     int32_t* req_state = reinterpret_cast<int32_t*>(ws + lay.req_state);
     uint64_t* anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
     int2* items = reinterpret_cast<int2*>(ws + lay.items);
-    float* part_out = (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
-    float* part_lse = (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+    float* part_out = range ? out : (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
+    float* part_lse = range ? lse : (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
     int32_t* tail_k = tail.cap > 0 ? reinterpret_cast<int32_t*>(ws + lay.tail_k) : nullptr;
 
     CUtensorMap map_lat, map_rope;
@@ -430,7 +436,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     pp.allow_unused_rows = graph_capture ? 1 : 0;
-    int32_t* merge_cnt = (splits == 2 || tail.cap > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    int32_t* merge_cnt =
+        !range && (splits == 2 || tail.cap > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
     pp.tail_k = tail_k;
     pp.tail_cap = tail.cap;
     pp.pairs = sm_count_of_current() / 2;
@@ -471,9 +478,10 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.max_pages = max_pages_per_seq;
     vp.num_pages = num_pages;
     vp.num_splits = splits;
-    vp.split_share = splits == 2 ? first_split_share(items_bound_of(batch, total_q, max_tree), item_tiles,
-                                                     sm_count_of_current() / 2)
-                                 : 0;
+    vp.split_share = splits == 2 && !range ? first_split_share(items_bound_of(batch, total_q, max_tree), item_tiles,
+                                                               sm_count_of_current() / 2)
+                                           : 0;   // a range of splits uses equal shares
+    vp.split_base = range ? split_begin : 0;
     vp.tail_cap = tail.cap;
     vp.tail_share = tail.share;
     vp.tail_k = tail_k;
@@ -484,7 +492,8 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.topk = topk;
     vp.kv = static_cast<const uint16_t*>(kv_cache);
     vp.merge_cnt = merge_cnt;
-    const dim3 grid(2u * static_cast<unsigned>(lay.max_items + tail.cap), static_cast<unsigned>(splits), 1u);
+    const dim3 grid(2u * static_cast<unsigned>(lay.max_items + tail.cap),
+                    static_cast<unsigned>(range ? split_count : splits), 1u);
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
     const bool merge = merge_cnt != nullptr;
@@ -496,6 +505,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     if (prof && cudaEventRecord(g_prof_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
 
     // ---- merge of the split partials (two splits are merged inside the verify kernel) ----
+    if (range) return MLA_OK;   // the caller merges the partials of all splits (mla_split_combine)
     if (splits > 2)
         return launch_combine(part_out, part_lse, splits, static_cast<long long>(total_q) * MLA_NUM_HEADS, out, lse,
                               stream);
@@ -510,6 +520,19 @@ int mla_verify_attn(const void* q_lat, const void* q_rope, const void* kv_cache,
     return verify_impl(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, out, lse, stream,
                        batch, total_q, max_tree, max_seq_len, num_heads, page_size, num_pages, max_pages_per_seq,
                        num_splits, workspace, workspace_bytes, nullptr, 0);
+}
+
+int mla_verify_attn_split_range(const void* q_lat, const void* q_rope, const void* kv_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, const int32_t* tree_parent,
+                                const int32_t* n_tree, float scale, float* part_out, float* part_lse,
+                                cudaStream_t stream, int batch, int total_q, int max_tree, int max_seq_len,
+                                int num_heads, int page_size, int num_pages, int max_pages_per_seq, int num_splits,
+                                int split_begin, int split_count, void* workspace, size_t workspace_bytes) {
+    if (split_count < 1) return MLA_ERR_INVALID_ARG;
+    return verify_impl(q_lat, q_rope, kv_cache, block_table, seq_lens, tree_parent, n_tree, scale, part_out, part_lse,
+                       stream, batch, total_q, max_tree, max_seq_len, num_heads, page_size, num_pages,
+                       max_pages_per_seq, num_splits, workspace, workspace_bytes, nullptr, 0, false, split_begin,
+                       split_count);
 }
 
 int mla_verify_sparse_num_splits(int batch, int total_q, int max_tree, int topk, int num_heads, int requested) {

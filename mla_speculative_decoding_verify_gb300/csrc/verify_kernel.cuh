@@ -113,6 +113,9 @@ struct VerifyParams {
     // part) and merged; their partials are compact: tail_cap row tiles per split
     int tail_cap, tail_share;
     const int32_t* tail_k;      // written by the prep kernel, or null
+    // this launch computes splits split_base .. split_base + gridDim.y - 1 of num_splits; their
+    // partials go to part_out / part_lse slots 0 .. gridDim.y - 1 (0 unless a range of splits is asked for)
+    int split_base;
     float scale_log2;           // softmax scale * log2(e)
     uint64_t timeout_ns;
     // sparse variant only
@@ -213,7 +216,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     grid_dependency_wait();     // the prep (and slot check) kernels' work list and metadata
     grid_launch_dependents();
     const int n_items = __ldg(p.item_count);
-    int item_slot = blockIdx.x >> 1, split = blockIdx.y, nsplit = p.num_splits, share = p.split_share;
+    int item_slot = blockIdx.x >> 1, split = blockIdx.y + p.split_base, nsplit = p.num_splits, share = p.split_share;
     int tail_j = -1;
     if (p.tail_k != nullptr) {
         const int k = min(min(__ldg(p.tail_k), p.tail_cap), n_items), whole = n_items - k;
@@ -398,13 +401,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         if (row_valid) {
             float* dst = (nsplit == 1)
                              ? p.out + grow * kDLatent + kDLatentHalf * c
-                             : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
-                                   kDLatentHalf * c;
+                             : p.part_out + (static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow) *
+                                       kDLatent + kDLatentHalf * c;
             for (int d = 0; d < kDLatentHalf; d += 4)
                 *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c == 0) {
                 if (nsplit == 1) p.lse[grow] = -INFINITY;
-                else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = -INFINITY;
+                else p.part_lse[static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow] = -INFINITY;
             }
         }
         return;
@@ -1017,8 +1020,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             float* dst = (nsplit == 1)
                              ? p.out + grow * kDLatent + kDLatentHalf * c
-                             : p.part_out + (static_cast<long long>(split) * p.total_q * kHeads + grow) * kDLatent +
-                                   kDLatentHalf * c;
+                             : p.part_out + (static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow) *
+                                       kDLatent + kDLatentHalf * c;
             // The rows go out through shared memory so that every store instruction
             // writes whole 128-byte lines: the thread of a row puts 32 of its values
             // into the warp's 4 KB tile (swizzled), then each lane stores 16 bytes of
@@ -1050,7 +1053,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
                 const float v = lse2 * 0.6931471805599453f;
                 if (nsplit == 1) p.lse[grow] = v;
-                else p.part_lse[static_cast<long long>(split) * p.total_q * kHeads + grow] = v;
+                else p.part_lse[static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow] = v;
             }
         }
     }

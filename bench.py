@@ -213,9 +213,11 @@ def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7, topk_idx=None)
 # The metric covers prefixes of 4k to 64k: after the headline workload the
 # default run measures these too (kernel time only), so that one bench line
 # records every configuration: name -> (workload, KV splits (0 = library's
-# choice), top-k slots for the sparse variant or None).
-SWEEP = {"c2": ("c2", 0, None), "c4_16splits": ("c4", 16, None), "c5": ("c5", 0, None),
-         "c3_sparse_top512": ("c3", 0, 512)}
+# choice, -1 = the persistent schedule), top-k slots for the sparse variant or
+# None).  c4 is taken both with 16 splits (its stated configuration) and with
+# the library's choice; c3 also on the persistent schedule.
+SWEEP = {"c2": ("c2", 0, None), "c4_16splits": ("c4", 16, None), "c4": ("c4", 0, None), "c5": ("c5", 0, None),
+         "c3_sparse_top512": ("c3", 0, 512), "c3_persistent": ("c3", -1, None)}
 
 
 def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dict:
@@ -273,8 +275,9 @@ def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dic
         status = binding.read_status(ws.data_ptr())
         k_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
         s_ms = sum(a.elapsed_time(b) for a, b in sev) / steps
-        units = int(((inp.n_tree + 1) // 2).sum() * splits)
-        traffic_key = f"{wl}/sparse-top{topk}" if topk else (f"{wl}/{splits}splits" if req else wl)
+        units = int(((inp.n_tree + 1) // 2).sum() * max(splits, 1))
+        traffic_key = (f"{wl}/sparse-top{topk}" if topk else f"{wl}/persistent" if req == -1
+                       else f"{wl}/{splits}splits" if req else wl)
         e = {"workload": inp.name, "num_splits": splits, "kernel_ms": k_ms, "step_ms": s_ms,
              "tflops": flops / (k_ms * 1e-3) / 1e12, "kv_gbps": kvb / (k_ms * 1e-3) / 1e9,
              "algorithmic_gflop": flops / 1e9, "device_status": status, "steps": steps,
@@ -508,7 +511,7 @@ def run_ours(args, ranks: Ranks):
     achieved = flops / (t_kern * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     # units of one launch = (row tile, split) work units
-    units = ((inp.n_tree + 1) // 2).sum() * splits
+    units = ((inp.n_tree + 1) // 2).sum() * max(splits, 1)
     traffic = profiled_traffic(f"{args.workload}/sparse-top{args.topk}" if sparse else args.workload, int(units))
     if sparse:
         gbs = kv_logical / (t_kern * 1e-3) / 1e9

@@ -60,6 +60,8 @@ typedef enum {
 #define MLA_D_ROPE 64
 #define MLA_MAX_TREE 64
 #define MLA_MAX_SPLITS 64
+/* num_splits value that asks for the persistent schedule (see mla_verify_num_splits) */
+#define MLA_SPLITS_PERSISTENT (-1)
 #define MLA_MAX_TOPK 2048
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -88,7 +90,16 @@ int mla_init(int device);
  * verify call may also cut the work items of its last, partial round of CTA
  * pairs in two and merge them in the kernel (decided on the device from the
  * exact item count); an explicit request of 1 never does.
- * Returns the count, or a negative mla_status on invalid arguments.
+ * `requested` = MLA_SPLITS_PERSISTENT asks for the persistent schedule instead:
+ * a fixed grid of 2-CTA clusters (as many as fit on the device at once), each
+ * taking an equal, contiguous share of the sequence of all (row tile, KV tile)
+ * pairs of the call and walking it with one pipeline across row tiles; a row
+ * tile cut between clusters is merged inside the verify kernel by the last of
+ * its pieces to finish, in piece order (the result does not depend on timing).
+ * The shares are cut on the device from the exact work, so a graph captured
+ * for a bucket computes exactly what the eager call computes.
+ * Returns the count, 0 for the persistent schedule, or a negative mla_status
+ * on invalid arguments.
  */
 int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
                           int num_heads, int requested);
@@ -96,8 +107,9 @@ int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
 /*
  * Bytes of device workspace mla_verify_attn needs for these sizes (with
  * `num_splits` resolved as by mla_verify_num_splits, including room for the
- * cut described there when `num_splits` is 0).  Pass the same `num_splits`
- * to mla_verify_attn.  0 on invalid input.
+ * cut described there when `num_splits` is 0, and for the pieces' partials
+ * when it is MLA_SPLITS_PERSISTENT: 2 x 128 rows x 512 fp32 per cluster).
+ * Pass the same `num_splits` to mla_verify_attn.  0 on invalid input.
  */
 size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_seq_len,
                                  int num_heads, int num_splits);
@@ -133,6 +145,7 @@ size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_s
  *              takes a shape-dependent share of each request's KV tiles (chosen
  *              so that the work units fill the SMs' rounds evenly); with more,
  *              a log-sum-exp combine pass follows the verify kernel.
+ *              MLA_SPLITS_PERSISTENT: the persistent schedule (no combine pass).
  *  workspace   device scratch of at least mla_verify_workspace_size(...) bytes,
  *              256-byte aligned; it holds the status word, the per-call tree
  *              metadata and, when split, the partial outputs.  Its contents

@@ -33,6 +33,7 @@ D_LATENT = 512
 D_ROPE = 64
 MAX_TREE = 64
 MAX_SPLITS = 64
+SPLITS_PERSISTENT = -1   # num_splits value asking for the persistent schedule
 MAX_TOPK = 2048
 
 EXPORTED = ("mla_version", "mla_error_string", "mla_init", "mla_verify_num_splits",
@@ -134,8 +135,9 @@ def init(device: int = 0) -> None:
 
 
 def num_splits(batch, total_q, max_tree, max_seq_len, num_heads=NUM_HEADS, requested=0) -> int:
+    """KV splits the verify call will use; 0 means the persistent schedule."""
     s = lib().mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, requested)
-    if s <= 0:
+    if s < 0:
         raise MlaError(-s, "mla_verify_num_splits")
     return int(s)
 
@@ -196,8 +198,9 @@ def set_profile_events(begin, end) -> None:
 
 
 def sparse_num_splits(batch, total_q, max_tree, topk, num_heads=NUM_HEADS, requested=0) -> int:
+    """KV splits the sparse verify call will use; 0 means the persistent schedule."""
     s = lib().mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, requested)
-    if s <= 0:
+    if s < 0:
         raise MlaError(-s, "mla_verify_sparse_num_splits")
     return int(s)
 

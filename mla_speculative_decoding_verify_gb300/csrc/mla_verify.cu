@@ -38,6 +38,7 @@ constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per pipeline wait
 struct DeviceState {
     bool ready = false;
     int sm_count = 0;
+    int pairs = 0;   // CTA pairs of the verify kernel that fit on the device at once
 };
 
 std::mutex g_mutex;
@@ -56,7 +57,7 @@ int current_device() {
 // Workspace layout shared by the size query and the launch.
 struct Layout {
     size_t status, item_count, q_off, req_state, order, item_off, anc, items, part_out, part_lse, tok_req, merge_cnt,
-        tail_k, total;
+        tail_k, woff, pair_begin, pair_item, item_first_pair, rounds, total;
     int max_items;
 };
 
@@ -82,7 +83,8 @@ TailPlan tail_plan(int tiles, int pairs, double merge_tiles) {
     return t;
 }
 
-Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, int tail_cap = 0) {
+// sched_pairs > 0: the persistent schedule on that many CTA pairs (num_splits is then 1 and tail_cap 0).
+Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, int tail_cap = 0, int sched_pairs = 0) {
     Layout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -101,7 +103,19 @@ Layout make_layout(int batch, int total_q, int num_splits, bool sparse = false, 
     L.items = take(sizeof(int2) * L.max_items);
     const size_t rows = static_cast<size_t>(total_q) * MLA_NUM_HEADS;
     L.part_out = L.part_lse = L.merge_cnt = L.tail_k = 0;
-    if (num_splits > 1) {
+    L.woff = L.pair_begin = L.pair_item = L.item_first_pair = L.rounds = 0;
+    if (sched_pairs > 0) {
+        // pieces of items cut between pairs: slots 2q (first segment of pair q) and 2q + 1 (its last)
+        const size_t slots = 2 * static_cast<size_t>(sched_pairs);
+        L.part_out = take(sizeof(float) * slots * mla::kRows * MLA_D_LATENT);
+        L.part_lse = take(sizeof(float) * slots * 2 * mla::kRows);
+        L.merge_cnt = take(sizeof(int32_t) * 4 * static_cast<size_t>(L.max_items));
+        L.woff = take(sizeof(long long) * (static_cast<size_t>(L.max_items) + 1));
+        L.pair_begin = take(sizeof(long long) * (static_cast<size_t>(sched_pairs) + 1));
+        L.pair_item = take(sizeof(int32_t) * (static_cast<size_t>(sched_pairs) + 1));
+        L.item_first_pair = take(sizeof(int32_t) * static_cast<size_t>(L.max_items));
+        L.rounds = take(sizeof(int32_t));
+    } else if (num_splits > 1) {
         L.part_out = take(sizeof(float) * rows * MLA_D_LATENT * num_splits);
         // two splits are merged in the verify kernel: lse per CTA half, and per-tile counters
         L.part_lse = take(sizeof(float) * rows * num_splits * (num_splits == 2 ? 2 : 1));
@@ -219,7 +233,39 @@ int first_split_share(long long items, int tiles, int pairs) {
     return share;
 }
 
-// Split count for requests of up to `tiles` KV tiles per row tile.
+int persistent_pairs();
+
+// Whole-item rounds of the persistent schedule for `items` work items on `pairs`
+// CTA pairs (the prep kernel's rule: a last round of fewer than pairs / 4 items
+// joins the round before, so that its items are not cut into many small pieces).
+long long persistent_rounds(long long items, int pairs) {
+    long long r = items / pairs;
+    if (r > 0 && items - r * pairs < pairs / 4) --r;
+    return r;
+}
+
+// Model of the persistent schedule's time, in the units of model_time: whole-item
+// rounds, then the rest shared evenly over the pairs with one more segment and a
+// merge per pair, every tile 1 % slower than on the per-unit grid (measured on
+// whole rounds of 16 x 16384-token items: 0.7-1.3 %).
+double persistent_model_time(long long items, int tiles, int pairs) {
+    const long long rounds = persistent_rounds(items, pairs);
+    const long long rest = items - rounds * pairs;
+    double t = static_cast<double>(rounds) * (tiles + kUnitOverheadTiles);
+    if (rest > 0) t += static_cast<double>(rest) * tiles / pairs + kUnitOverheadTiles + kMergeTiles;
+    return 1.01 * t;
+}
+
+// Split count for requests of up to `tiles` KV tiles per row tile, or 0 for the
+// persistent schedule.  Sizes are bounds (the host never reads device data), so
+// the model takes every item as `tiles` long.  The persistent schedule is taken
+// only when every request has max_tree tree tokens (total_q = batch x max_tree:
+// then the item count is exact, and the rounds the model counts are the real
+// ones), with at least one round of whole items (with none, pairs stream one
+// request's KV at different offsets and lose its reuse in L2; measured 1-3 %
+// slower), and when the model puts it at least 5 % ahead.  Measured on 2048- to
+// 32768-token prefixes, it was 2-8 % faster where the per-unit grid's last round
+// was too large to cut in two, and 2-7 % slower elsewhere.
 int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
     const long long items_bound = items_bound_of(batch, total_q, max_tree);
     const int pairs = sm_count_of_current() / 2;
@@ -234,6 +280,11 @@ int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
             best = s;
         }
     }
+    const int pp = persistent_pairs();
+    const bool exact = static_cast<long long>(batch) * max_tree == total_q;
+    if (exact && persistent_rounds(items_bound, pp) >= 1 &&
+        persistent_model_time(items_bound, tiles, pp) < 0.95 * best_t)
+        return 0;
     return best;
 }
 
@@ -243,6 +294,20 @@ int choose_splits(int batch, int total_q, int max_tree, int max_seq_len) {
 
 // KV tiles of a sparse row tile: two tokens' slot lists, then the tree keys.
 int sparse_tiles(int topk) { return 2 * ((topk + mla::kBlockN - 1) / mla::kBlockN) + 1; }
+
+// Persistent schedule: a share is moved to an item boundary rather than leave a
+// piece of fewer tiles than this (a piece costs a q load, a pipeline fill and a merge).
+constexpr int kMinPieceTiles = 4;
+
+// CTA pairs of the persistent schedule: every pair of the device, whatever the
+// sizes (the shares are cut from the exact work on the device; a pair whose share
+// is empty exits at once).  The partition, and so the result, then depends only on
+// the requests, not on the buffer sizes a graph was captured for.
+int persistent_pairs() {
+    const int d = current_device();
+    if (d >= 0 && d < kMaxDevices && g_dev[d].ready && g_dev[d].pairs > 0) return g_dev[d].pairs;
+    return std::max(1, sm_count_of_current() / 2);
+}
 
 // Tail cut of a launch whose split count was chosen automatically as one (an
 // explicit request is taken as it is).  `tiles` = KV tiles of a work item.
@@ -345,21 +410,39 @@ int mla_init(int device) {
     if (cudaFuncSetAttribute(mla::mla_tree_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(mla::kAcceptSmemBytes)) != cudaSuccess)
         return MLA_ERR_CUDA;
-    for (const void* fn : {reinterpret_cast<const void*>(mla::mla_verify_kernel<false, false>),
-                           reinterpret_cast<const void*>(mla::mla_verify_kernel<false, true>),
-                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, false>),
-                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, true>)})
+    for (const void* fn : {reinterpret_cast<const void*>(mla::mla_verify_kernel<false, mla::kSchedPlain>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<false, mla::kSchedMerge>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<false, mla::kSchedPersistent>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedPlain>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedMerge>),
+                           reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedPersistent>)})
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mla::kSmemBytes)) !=
             cudaSuccess)
             return MLA_ERR_CUDA;
     g_dev[device].sm_count = prop.multiProcessorCount;
+    // 2-CTA clusters of the verify kernel resident at once (one CTA per SM; the
+    // placement of clusters may leave SMs out), the grid of the persistent schedule
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2u * static_cast<unsigned>(std::max(1, prop.multiProcessorCount / 2)));
+        cfg.blockDim = dim3(mla::kThreadsSparse);
+        cfg.dynamicSmemBytes = mla::kSmemBytes;
+        int clusters = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(
+            &clusters, reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedPersistent>), &cfg);
+        if (e != cudaSuccess) cudaGetLastError();   // not fatal: fall back to half the SMs
+        const int half = std::max(1, prop.multiProcessorCount / 2);
+        g_dev[device].pairs = (e == cudaSuccess && clusters > 0) ? std::min(clusters, half) : half;
+    }
     g_dev[device].ready = true;
     return MLA_OK;
 }
 
 int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len, int num_heads, int requested) {
-    if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || requested < 0) return -MLA_ERR_INVALID_ARG;
+    if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || requested < MLA_SPLITS_PERSISTENT)
+        return -MLA_ERR_INVALID_ARG;
     if (num_heads != MLA_NUM_HEADS) return -MLA_ERR_UNSUPPORTED;
+    if (requested == MLA_SPLITS_PERSISTENT) return 0;
     if (requested > 0) return std::min(requested, MLA_MAX_SPLITS);
     return choose_splits(batch, total_q, max_tree, max_seq_len);
 }
@@ -367,8 +450,10 @@ int mla_verify_num_splits(int batch, int total_q, int max_tree, int max_seq_len,
 size_t mla_verify_workspace_size(int batch, int total_q, int max_tree, int max_seq_len, int num_heads,
                                  int num_splits) {
     const int s = mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
-    if (s <= 0) return 0;
-    const TailPlan tp = launch_tail_plan(false, (max_seq_len + mla::kBlockN - 1) / mla::kBlockN, num_splits, s);
+    if (s < 0) return 0;
+    const int tiles = (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
+    if (s == 0) return make_layout(batch, total_q, 1, false, 0, persistent_pairs()).total;
+    const TailPlan tp = launch_tail_plan(false, tiles, num_splits, s);
     return make_layout(batch, total_q, s, false, tp.cap).total;
 }
 
@@ -386,7 +471,7 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
         return num_splits > MLA_MAX_SPLITS ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
     // ---- host-checkable arguments ----
     if (batch < 0 || total_q < 0 || max_tree < 0 || max_seq_len < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
-        num_splits < 0 || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
+        num_splits < MLA_SPLITS_PERSISTENT || page_size <= 0 || !std::isfinite(scale) || !(scale > 0.f))
         return MLA_ERR_INVALID_ARG;
     if (num_heads != MLA_NUM_HEADS || page_size % mla::kBlockN != 0 || max_tree > MLA_MAX_TREE ||
         num_splits > MLA_MAX_SPLITS)
@@ -400,13 +485,17 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     if (num_pages == 0 || max_pages_per_seq == 0) return MLA_ERR_INVALID_ARG;
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MLA_ERR_NOT_INITIALIZED;
-    const int splits = topk > 0 ? mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits)
-                                : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
-    if (splits <= 0) return MLA_ERR_INVALID_ARG;
+    const int resolved = topk > 0 ? mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits)
+                                  : mla_verify_num_splits(batch, total_q, max_tree, max_seq_len, num_heads, num_splits);
+    if (resolved < 0) return MLA_ERR_INVALID_ARG;
+    const bool persistent = resolved == 0 && !range;   // 0: the persistent schedule
+    if (resolved == 0 && range) return MLA_ERR_INVALID_ARG;
+    const int splits = persistent ? 1 : resolved;
     const int item_tiles = topk > 0 ? sparse_tiles(topk) : (max_seq_len + mla::kBlockN - 1) / mla::kBlockN;
-    const TailPlan tail = range ? TailPlan{} : launch_tail_plan(topk > 0, item_tiles, num_splits, splits);
+    const int sched_pairs = persistent ? persistent_pairs() : 0;
+    const TailPlan tail = (range || persistent) ? TailPlan{} : launch_tail_plan(topk > 0, item_tiles, num_splits, splits);
     // a range of splits writes its partials to the caller's buffers: no partials in the workspace
-    const Layout lay = make_layout(batch, total_q, range ? 1 : splits, topk > 0, tail.cap);
+    const Layout lay = make_layout(batch, total_q, range ? 1 : splits, topk > 0, tail.cap, sched_pairs);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_WORKSPACE;
 
@@ -417,8 +506,9 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     int32_t* req_state = reinterpret_cast<int32_t*>(ws + lay.req_state);
     uint64_t* anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
     int2* items = reinterpret_cast<int2*>(ws + lay.items);
-    float* part_out = range ? out : (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
-    float* part_lse = range ? lse : (splits > 1 || tail.cap > 0) ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
+    const bool ws_parts = splits > 1 || tail.cap > 0 || persistent;
+    float* part_out = range ? out : ws_parts ? reinterpret_cast<float*>(ws + lay.part_out) : nullptr;
+    float* part_lse = range ? lse : ws_parts ? reinterpret_cast<float*>(ws + lay.part_lse) : nullptr;
     int32_t* tail_k = tail.cap > 0 ? reinterpret_cast<int32_t*>(ws + lay.tail_k) : nullptr;
 
     CUtensorMap map_lat, map_rope;
@@ -448,13 +538,27 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     pp.max_items = lay.max_items;
     pp.tok_req = topk > 0 ? reinterpret_cast<int32_t*>(ws + lay.tok_req) : nullptr;
     pp.allow_unused_rows = graph_capture ? 1 : 0;
-    int32_t* merge_cnt =
-        !range && (splits == 2 || tail.cap > 0) ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt) : nullptr;
+    int32_t* merge_cnt = !range && (splits == 2 || tail.cap > 0 || persistent)
+                             ? reinterpret_cast<int32_t*>(ws + lay.merge_cnt)
+                             : nullptr;
     pp.tail_k = tail_k;
     pp.tail_cap = tail.cap;
     pp.pairs = sm_count_of_current() / 2;
     pp.zero_words = merge_cnt;
     pp.zero_count = merge_cnt ? 4 * lay.max_items : 0;
+    long long* woff = persistent ? reinterpret_cast<long long*>(ws + lay.woff) : nullptr;
+    long long* pair_begin = persistent ? reinterpret_cast<long long*>(ws + lay.pair_begin) : nullptr;
+    int32_t* pair_item = persistent ? reinterpret_cast<int32_t*>(ws + lay.pair_item) : nullptr;
+    int32_t* item_first_pair = persistent ? reinterpret_cast<int32_t*>(ws + lay.item_first_pair) : nullptr;
+    int32_t* rounds = persistent ? reinterpret_cast<int32_t*>(ws + lay.rounds) : nullptr;
+    pp.rounds = rounds;
+    pp.woff = woff;
+    pp.pair_begin = pair_begin;
+    pp.pair_item = pair_item;
+    pp.item_first_pair = item_first_pair;
+    pp.sched_pairs = sched_pairs;
+    pp.min_piece = kMinPieceTiles;
+    pp.topk = topk;
     mla::mla_prep_kernel<<<1, mla::kPrepThreads, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (topk > 0) {
@@ -504,13 +608,23 @@ static int verify_impl(const void* q_lat, const void* q_rope, const void* kv_cac
     vp.topk = topk;
     vp.kv = static_cast<const uint16_t*>(kv_cache);
     vp.merge_cnt = merge_cnt;
-    const dim3 grid(2u * static_cast<unsigned>(lay.max_items + tail.cap),
+    vp.woff = woff;
+    vp.pair_begin = pair_begin;
+    vp.pair_item = pair_item;
+    vp.item_first_pair = item_first_pair;
+    vp.rounds = rounds;
+    vp.pairs = sched_pairs;
+    const dim3 grid(2u * static_cast<unsigned>(persistent ? sched_pairs : lay.max_items + tail.cap),
                     static_cast<unsigned>(range ? split_count : splits), 1u);
     const bool prof = !graph_capture && g_prof_begin && g_prof_end;
     if (prof && cudaEventRecord(g_prof_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
-    const bool merge = merge_cnt != nullptr;
-    auto* kernel = topk > 0 ? (merge ? mla::mla_verify_kernel<true, true> : mla::mla_verify_kernel<true, false>)
-                            : (merge ? mla::mla_verify_kernel<false, true> : mla::mla_verify_kernel<false, false>);
+    const int sched = persistent ? mla::kSchedPersistent : merge_cnt != nullptr ? mla::kSchedMerge : mla::kSchedPlain;
+    auto* kernel = topk > 0 ? (sched == mla::kSchedPersistent ? mla::mla_verify_kernel<true, mla::kSchedPersistent>
+                               : sched == mla::kSchedMerge    ? mla::mla_verify_kernel<true, mla::kSchedMerge>
+                                                              : mla::mla_verify_kernel<true, mla::kSchedPlain>)
+                            : (sched == mla::kSchedPersistent ? mla::mla_verify_kernel<false, mla::kSchedPersistent>
+                               : sched == mla::kSchedMerge    ? mla::mla_verify_kernel<false, mla::kSchedMerge>
+                                                              : mla::mla_verify_kernel<false, mla::kSchedPlain>);
     if (launch_dependent(kernel, grid, dim3(topk > 0 ? mla::kThreadsSparse : mla::kThreads), mla::kSmemBytes, stream,
                          vp, map_lat, map_rope) != cudaSuccess)
         return MLA_ERR_CUDA;
@@ -548,8 +662,10 @@ int mla_verify_attn_split_range(const void* q_lat, const void* q_rope, const voi
 }
 
 int mla_verify_sparse_num_splits(int batch, int total_q, int max_tree, int topk, int num_heads, int requested) {
-    if (batch < 0 || total_q < 0 || max_tree < 0 || requested < 0 || topk < 1) return -MLA_ERR_INVALID_ARG;
+    if (batch < 0 || total_q < 0 || max_tree < 0 || requested < MLA_SPLITS_PERSISTENT || topk < 1)
+        return -MLA_ERR_INVALID_ARG;
     if (num_heads != MLA_NUM_HEADS || topk > MLA_MAX_TOPK) return -MLA_ERR_UNSUPPORTED;
+    if (requested == MLA_SPLITS_PERSISTENT) return 0;
     if (requested > 0) return std::min(requested, MLA_MAX_SPLITS);
     return choose_splits_tiles(batch, total_q, max_tree, sparse_tiles(topk));
 }
@@ -557,7 +673,9 @@ int mla_verify_sparse_num_splits(int batch, int total_q, int max_tree, int topk,
 size_t mla_verify_sparse_workspace_size(int batch, int total_q, int max_tree, int topk, int num_heads,
                                         int num_splits) {
     const int s = mla_verify_sparse_num_splits(batch, total_q, max_tree, topk, num_heads, num_splits);
-    if (s <= 0) return 0;
+    if (s < 0) return 0;
+    if (s == 0)
+        return make_layout(batch, total_q, 1, true, 0, persistent_pairs()).total;
     const TailPlan tp = launch_tail_plan(true, sparse_tiles(topk), num_splits, s);
     return make_layout(batch, total_q, s, true, tp.cap).total;
 }

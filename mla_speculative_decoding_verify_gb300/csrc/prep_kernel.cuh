@@ -1,9 +1,11 @@
 // Per-call metadata for the verify kernel: query offsets of the requests,
 // the ancestor-or-self bit set of every draft-tree node, input validation
-// into the status word, and the list of (request, row tile) work items in
-// longest-request-first order.  One thread block; integer work only.  Each
-// request is handled by one warp (its tree fits in two words per lane), so
-// no thread walks a long chain of dependent global loads.
+// into the status word, the list of (request, row tile) work items in
+// longest-request-first order, and, for the persistent schedule, each CTA
+// pair's share of the sequence of all (item, KV tile) positions.  One thread
+// block; integer work only.  Each request is handled by one warp (its tree
+// fits in two words per lane), so no thread walks a long chain of dependent
+// global loads.
 #pragma once
 
 #include <cstdint>
@@ -37,36 +39,49 @@ struct PrepParams {
     int zero_count;
     int32_t* tail_k;             // one split: how many items of the last, partial round to cut in two, or null
     int tail_cap, pairs;         // at most tail_cap; CTA pairs of the device
+    // persistent schedule (else null): item i holds positions [woff[i], woff[i + 1]) of the
+    // sequence of all (item, KV tile) pairs, one position per KV tile (an invalid request's
+    // item: one position and no tiles).  The first *rounds x sched_pairs items go whole,
+    // one per CTA pair and round; CTA pair q takes positions [pair_begin[q], pair_begin[q + 1])
+    // of the remaining items, an equal share moved to an item boundary when it would leave
+    // a piece of fewer than min_piece tiles
+    long long* woff;             // [max_items + 1]
+    long long* pair_begin;       // [sched_pairs + 1]
+    int32_t* pair_item;          // [sched_pairs + 1] item holding pair_begin[q] (item count at the end)
+    int32_t* item_first_pair;    // [max_items] first pair whose share holds a position of the item
+    int32_t* rounds;             // [1]
+    int sched_pairs, min_piece;
+    int topk;                    // sparse variant: slots per tree token (0 for the dense verify)
 };
 
 // Exclusive block-wide scan of f(i) for i in [0, n) into dst[0..n] (dst[n] = total).
-template <typename F>
-__device__ void block_exclusive_scan(int n, F f, int32_t* dst, int32_t* warp_sums) {
+template <typename T, typename F>
+__device__ void block_exclusive_scan(int n, F f, T* dst, T* warp_sums) {
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5;
-    int carry = 0;
+    T carry = 0;
     for (int base = 0; base < n; base += kPrepThreads) {
         const int i = base + tid;
-        const int v = i < n ? f(i) : 0;
-        int x = v;
+        const T v = i < n ? static_cast<T>(f(i)) : T(0);
+        T x = v;
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const T y = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += y;
         }
         if (lane == 31) warp_sums[wid] = x;
         __syncthreads();
         if (wid == 0) {
-            int w = warp_sums[lane];
+            T w = warp_sums[lane];
             for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                const T y = __shfl_up_sync(0xffffffffu, w, o);
                 if (lane >= o) w += y;
             }
             warp_sums[lane] = w;  // inclusive over warps
         }
         __syncthreads();
-        const int before = (wid > 0 ? warp_sums[wid - 1] : 0) + x - v;
+        const T before = (wid > 0 ? warp_sums[wid - 1] : T(0)) + x - v;
         if (i < n) dst[i] = carry + before;
-        const int chunk_total = warp_sums[31];
+        const T chunk_total = warp_sums[31];
         __syncthreads();
         carry += chunk_total;
     }
@@ -77,6 +92,7 @@ __device__ void block_exclusive_scan(int n, F f, int32_t* dst, int32_t* warp_sum
 __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepParams p) {
     grid_launch_dependents();   // the verify kernel may start its launch; it waits for this grid's results
     __shared__ int32_t warp_sums[32];
+    __shared__ long long warp_sums64[32];
     __shared__ int32_t tree_par[kPrepWarps][kMaxTree];
     __shared__ uint64_t tree_anc[kPrepWarps][kMaxTree];
     const int tid = threadIdx.x;
@@ -213,6 +229,72 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
             *p.tail_k = (rem > 0 && 2 * rem <= p.pairs) ? min(rem, p.tail_cap) : 0;
         }
         if (p.item_off[p.batch] > p.max_items) atomicOr(p.status, kStatusBadTree);
+    }
+
+    // 4. persistent schedule: the CTA pairs' shares of all (item, KV tile) positions
+    if (p.woff) {
+        __syncthreads();   // the work items written above
+        const int n = total_items;
+        block_exclusive_scan(
+            n,
+            [&](int k) -> long long {
+                const int2 it = p.items[k];
+                const int b = it.x;
+                if (p.req_state[b] != 0) return 1;   // rows written as out = 0, lse = -inf; no tiles
+                const int T = p.n_tree[b];
+                if (p.topk > 0) {
+                    const int nA = (p.topk + kBlockN - 1) / kBlockN;
+                    const int ntok = min(kTokensPerTile, T - kTokensPerTile * it.y);
+                    return static_cast<long long>(nA) * (ntok > 1 ? 2 : 1) + (T + kBlockN - 1) / kBlockN;
+                }
+                return (p.seq_lens[b] + kBlockN - 1) / kBlockN;
+            },
+            p.woff, warp_sums64);
+        const long long W = p.woff[n];
+        const int G = p.sched_pairs;
+        // Rounds of whole items first (the row tiles of a request then stream its KV
+        // together, sharing it in L2); the last, partial round is shared out evenly.  A
+        // partial round of fewer than G / 4 items joins the one before, so that its
+        // items are not cut into many small pieces.
+        int R = n / G;
+        if (R > 0 && n - R * G < G / 4) --R;
+        const long long X0 = p.woff[R * G], Wt = W - X0;
+        if (tid == 0) *p.rounds = R;
+        for (int q = tid; q <= G; q += kPrepThreads) {
+            long long x = X0 + (q >= G ? Wt : Wt * q / G);
+            int i = n;
+            if (x < W) {
+                int lo = 0, hi = n - 1;   // the item holding x: the last i with woff[i] <= x
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (p.woff[mid] <= x) lo = mid;
+                    else hi = mid - 1;
+                }
+                i = lo;
+                if (q > 0) {
+                    const long long O = p.woff[i], E = p.woff[i + 1];
+                    if (x - O < p.min_piece) {
+                        x = O;
+                    } else if (E - x < p.min_piece) {
+                        x = E;
+                        ++i;
+                    }
+                }
+            }
+            p.pair_begin[q] = x;
+            p.pair_item[q] = i;
+        }
+        __syncthreads();
+        for (int i = R * G + tid; i < n; i += kPrepThreads) {
+            const long long O = p.woff[i];
+            int lo = 0, hi = G - 1;   // the first pair whose share ends after O
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (p.pair_begin[mid + 1] > O) hi = mid;
+                else lo = mid + 1;
+            }
+            p.item_first_pair[i] = lo;
+        }
     }
 }
 

@@ -1,8 +1,8 @@
 // Fused tree-verify MLA attention kernel for sm_103a.
 //
 // One 2-CTA cluster computes 128 output rows (2 tree tokens x 64 heads) of one
-// request over one KV split.  The pair divides the work along the feature
-// axis: CTA c owns latent dims [256c, 256c+256) and rope dims [32c, 32c+32).
+// request over a range of its KV tiles.  The pair divides the work along the
+// feature axis: CTA c owns latent dims [256c, 256c+256) and rope dims [32c, 32c+32).
 //   - QK^T: each CTA multiplies its half of q by its half of every key
 //     (tcgen05, q latent half resident in TMEM, keys streamed by TMA), giving
 //     a partial score tile; the partials are exchanged through distributed
@@ -29,9 +29,18 @@
 // token's slots.  Two TMA warps gather the rows with four-row tensor gathers
 // into the same swizzled stage layout (empty slots read as zeros) and record
 // which of the tile's 64 slots are real.
-// Split KV: a work unit covers a range of a row tile's KV tiles (with two
-// splits, a host-chosen share for the first); two splits are merged here by
-// the second unit of each row tile to finish, more by a separate combine pass.
+// Schedules (template parameter kSched):
+//   - per-unit grid (kSchedPlain, kSchedMerge): one CTA pair per work unit, a
+//     range of one row tile's KV tiles (split KV, flash-decoding style); two
+//     splits are merged here by the second unit of each row tile to finish,
+//     more by a separate combine pass;
+//   - persistent (kSchedPersistent): a fixed grid of CTA pairs, each taking an
+//     equal, contiguous share of the sequence of all (work item, KV tile)
+//     positions.  A pair walks its share item by item with one pipeline:
+//     barriers, TMEM and the cluster stay alive, the KV ring keeps streaming
+//     across item boundaries.  An item cut between two or more pairs is merged
+//     in the kernel by the last of its pieces to finish (LSE weights, summed in
+//     piece order so that the result does not depend on the order of arrival).
 // TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
 #pragma once
 
@@ -78,9 +87,12 @@ static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 102
 static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
 // the two-split merge copies the other split's 128 rows x 1 KB over the stages, q rope and receive buffer
 static_assert(kOffStaging - kOffStages >= kRows * kDLatentHalf * 4, "merge buffer");
+// the q staging and the persistent merge use the staging and P buffers as one 64 KB region, 16 KB per warp
+static_assert(kOffP == kOffStaging + kXBufBytes && kXBufBytes + 2 * kPBytes >= 4 * 16384, "staging region");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // S buffer x at kTmS + 64 * x
+constexpr uint32_t kTmAcc = 256;   // persistent merge: accumulator over the q and S columns (free in an epilogue)
 
 constexpr float kLazyRescaleLog2 = 8.0f;   // rescale only when the max grows by > 2^8
 constexpr float kLowPartShare = 1.0f / 16.0f;
@@ -90,6 +102,11 @@ constexpr int kStatusTimeout = 1 << 5;
 constexpr int kStatusBadTree = 1 << 6;
 constexpr int kStatusBadBlock = 1 << 7;
 constexpr int kStatusBadIndex = 1 << 9;
+
+// Schedules of the verify kernel.
+constexpr int kSchedPlain = 0;        // one work unit per CTA pair; more than one split goes to the combine pass
+constexpr int kSchedMerge = 1;        // the same, and two-split / cut units merged in the kernel
+constexpr int kSchedPersistent = 2;   // a fixed grid of CTA pairs, each walking its share of all KV tiles
 
 struct VerifyParams {
     const uint16_t* q_lat;      // [total_q, 64, 512]
@@ -105,8 +122,8 @@ struct VerifyParams {
     int* status;                // [1]
     float* out;                 // [total_q, 64, 512]
     float* lse;                 // [total_q, 64]
-    float* part_out;            // [num_splits, total_q * 64, 512]
-    float* part_lse;            // [num_splits, total_q * 64]
+    float* part_out;            // per-unit grid: [num_splits, total_q * 64, 512]; persistent: [2 * pairs, 128, 512]
+    float* part_lse;            // per-unit grid: [num_splits, total_q * 64]; persistent: [2 * pairs, 2, 128]
     int batch, total_q, page_size, max_pages, num_pages, num_splits, max_items;
     int split_share;            // two splits: the first one's share of a work item's tiles, in 1/1024 (0 = halves)
     // one split, but the last *tail_k (<= tail_cap) work items cut in two (tail_share for the first
@@ -121,9 +138,20 @@ struct VerifyParams {
     // sparse variant only
     const int32_t* topk_idx;    // [total_q, topk] prefix positions, -1 = unused slot
     const uint16_t* kv;         // the cache [num_pages * page_size, 576] (L2 prefetch of gathered rows)
-    // exactly two KV splits: merged in the kernel (else null and a separate combine runs)
-    int32_t* merge_cnt;         // [max_items][2 halves][arrived, written], zeroed by the prep kernel
+    // two KV splits or cut items merged in the kernel: [max_items][2 halves][arrived, written],
+    // zeroed by the prep kernel (else null)
+    int32_t* merge_cnt;
     int topk;
+    // persistent schedule (written by the prep kernel; else null).  Position x of the
+    // sequence of all (work item, KV tile) pairs: item i holds [woff[i], woff[i + 1]).
+    // Items 0 .. *rounds * pairs - 1 go whole, one per CTA pair and round (snake
+    // order); the positions of the others are shared out.
+    const long long* woff;        // [items + 1]
+    const long long* pair_begin;  // [pairs + 1] first position of each CTA pair's share
+    const int32_t* pair_item;     // [pairs + 1] item holding that position
+    const int32_t* item_first_pair;  // [items] first CTA pair whose share holds a tile of the item
+    const int32_t* rounds;        // [1]
+    int pairs;
 };
 
 struct Ctrl {
@@ -137,7 +165,7 @@ struct Ctrl {
     uint64_t x_full;       // the peer's partial of the next tile landed in the receive buffer (bytes)
     uint64_t x_empty;      // the peer finished reading the partial this CTA sent it
     uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
-    uint64_t q_ready;
+    uint64_t q_ready;      // q of the next segment is in TMEM / shared memory (one phase per segment)
     uint64_t drain_qk;
     uint64_t drain_pv;
     uint64_t never;        // fault injection: nothing arrives on it
@@ -145,7 +173,7 @@ struct Ctrl {
     int abort;
     int lo_flag[2];
     int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
-    int merge_role;     // two-split merge: 0 = first of the row tile's two units here, 1 = second
+    int merge_role;     // in-kernel merge: arrival rank of this unit / piece among the row tile's
     uint32_t slot_mask[kStages][2];  // sparse: bit k of half h set if key 32h + k of the stage's tile is a real slot
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -154,12 +182,14 @@ __device__ __forceinline__ void raise_status(int* status, int bit) { atomicOr(st
 
 // Fault injection (a test build only, compiled with MLA_FAULT_INJECTION): make
 // one bounded wait run out so that the timeout paths can be tested without
-// faulting or hanging the GPU.  Kinds, all in the first work unit (item 0,
-// split 0) and CTA 0 of its pair:
+// faulting or hanging the GPU.  Kinds, all in the first segment of work item 0
+// (split 0) and CTA 0 of its pair:
 //   1  the QK issuer waits for KV tile 1 on a barrier that nothing completes;
 //   2  (two splits merged in the kernel) the first unit of the row tile never
 //      marks its partial written, so the second one's poll runs out;
-//   3  the softmax threads do not send the partial scores of tile 1.
+//   3  the softmax threads do not send the partial scores of tile 1;
+//   4  (persistent schedule) the pieces of cut items other than the last never
+//      mark their partials written, so the last one's poll runs out.
 #ifdef MLA_FAULT_INJECTION
 __device__ int g_fault_kind;
 __device__ __forceinline__ int fault_kind() { return *reinterpret_cast<volatile int*>(&g_fault_kind); }
@@ -195,12 +225,141 @@ __device__ __forceinline__ void sparse_segment(int j, int nA, int nB, int& kind,
     }
 }
 
-// kMerge: the variant that can merge two splits in the kernel (its code is
-// kept out of the plain variant: small launches run every path cold).
+// ---- segments: the pieces of work a CTA pair computes ----
+// Output of a segment.
+constexpr int kOutFinal = 0;      // the whole item: normalised rows into out / lse
+constexpr int kOutPartial = 1;    // one split of a per-unit grid: normalised partial into its split slot
+constexpr int kOutTwoSplit = 2;   // per-unit grid: two-split or cut unit, merged in the kernel
+constexpr int kOutPiece = 3;      // persistent: a piece of an item cut between CTA pairs, merged in the kernel
+
+// KV tiles [t0, t0 + n) of one work item (identical in both CTAs of the pair).
+struct Seg {
+    int item;          // index into the work list
+    int b;             // request
+    int T, L, P;       // tree tokens, KV rows and prefix length of the request
+    int qbase, ntok;   // first tree token of the row tile, tokens in it (1 or 2)
+    int nA, nB;        // sparse: KV tiles of token 0's and token 1's slot lists
+    int t0, n;         // first KV tile (of the item's key sequence) and tile count
+    int kind;          // kOut*
+    int split;         // per-unit grid: split of the item; persistent: 0
+    int tail_j;        // per-unit grid, cut item: its compact partial slot; else -1
+    bool bad;          // invalid request: no tiles, rows written as out = 0, lse = -inf
+};
+
+// Where the next segment comes from.
+struct Cursor {
+    long long x, end;  // persistent: next position of the pair's share, end of the share
+    int item;          // persistent: item holding x
+    int round, rounds; // persistent: whole-item rounds handed out, and their number
+    int pair;          // persistent: this CTA pair
+    bool done;         // per-unit grid: the one segment was handed out
+};
+
+template <bool kSparse>
+__device__ __forceinline__ void seg_item(const VerifyParams& p, int item, Seg& s) {
+    const int2 it = p.items[item];
+    s.item = item;
+    s.b = it.x;
+    s.T = __ldg(p.n_tree + s.b);
+    s.L = __ldg(p.seq_lens + s.b);
+    s.P = s.L - s.T;
+    s.qbase = __ldg(p.q_off + s.b) + kTokensPerTile * it.y;
+    s.ntok = min(kTokensPerTile, s.T - kTokensPerTile * it.y);
+    s.bad = __ldg(p.req_state + s.b) != 0;
+    s.nA = s.nB = 0;
+    if constexpr (kSparse) {
+        s.nA = (p.topk + kBlockN - 1) / kBlockN;
+        s.nB = s.ntok > 1 ? s.nA : 0;
+    }
+}
+
+// KV tiles of the item's key sequence (0 for an invalid request).
+template <bool kSparse>
+__device__ __forceinline__ int item_kv_tiles(const Seg& s) {
+    return s.bad ? 0 : (kSparse ? s.nA + s.nB + (s.T + kBlockN - 1) / kBlockN : (s.L + kBlockN - 1) / kBlockN);
+}
+
+// Per-unit grid: the unit of this CTA pair, from blockIdx.  Regular: one unit
+// per (item, blockIdx.y).  With k = *tail_k > 0 the whole items come first,
+// then the first parts of the last k items, then their second parts; tail_j
+// numbers a cut item among the k.
 template <bool kSparse, bool kMerge>
+__device__ __forceinline__ bool unit_segment(const VerifyParams& p, int n_items, Seg& s) {
+    int item = blockIdx.x >> 1, split = blockIdx.y + p.split_base, nsplit = p.num_splits, share = p.split_share;
+    int tail_j = -1;
+    if (p.tail_k != nullptr) {
+        const int k = min(min(__ldg(p.tail_k), p.tail_cap), n_items), whole = n_items - k;
+        if (k > 0 && item >= whole) {
+            const int j = item - whole;
+            if (j >= 2 * k) return false;
+            tail_j = j % k;
+            item = whole + tail_j;
+            split = j / k;
+            nsplit = 2;
+            share = p.tail_share;
+        }
+    }
+    if (item >= n_items) return false;
+    seg_item<kSparse>(p, item, s);
+    int t0, t1;
+    split_range(item_kv_tiles<kSparse>(s), split, nsplit, share, t0, t1);
+    s.t0 = t0;
+    s.n = t1 - t0;
+    s.split = split;
+    s.tail_j = tail_j;
+    s.kind = (kMerge && p.merge_cnt != nullptr && nsplit == 2) ? kOutTwoSplit
+             : nsplit == 1                                      ? kOutFinal
+                                                                : kOutPartial;
+    return true;
+}
+
+// Persistent schedule: the pair's whole item of the next round, then the next
+// item piece of its share [x, end) of the remaining items.
+template <bool kSparse>
+__device__ __forceinline__ bool share_segment(const VerifyParams& p, int n_items, Cursor& cu, Seg& s) {
+    if (cu.round < cu.rounds) {
+        const int r = cu.round++;
+        seg_item<kSparse>(p, r * p.pairs + ((r & 1) ? p.pairs - 1 - cu.pair : cu.pair), s);
+        s.t0 = 0;
+        s.n = item_kv_tiles<kSparse>(s);
+        s.split = 0;
+        s.tail_j = -1;
+        s.kind = kOutFinal;
+        return true;
+    }
+    if (cu.x >= cu.end || cu.item >= n_items) return false;
+    const long long O = __ldg(p.woff + cu.item), E = __ldg(p.woff + cu.item + 1);
+    seg_item<kSparse>(p, cu.item, s);
+    const long long a = cu.x - O, e = min(cu.end, E) - O;
+    const long long nkv = item_kv_tiles<kSparse>(s);
+    s.t0 = static_cast<int>(min(a, nkv));
+    s.n = static_cast<int>(min(e, nkv)) - s.t0;
+    s.split = 0;
+    s.tail_j = -1;
+    s.kind = (a == 0 && O + e == E) ? kOutFinal : kOutPiece;
+    cu.x = O + e;
+    ++cu.item;
+    return true;
+}
+
+template <bool kSparse, int kSched>
+__device__ __forceinline__ bool next_segment(const VerifyParams& p, int n_items, Cursor& cu, Seg& s) {
+    if constexpr (kSched == kSchedPersistent) {
+        return share_segment<kSparse>(p, n_items, cu, s);
+    } else {
+        if (cu.done) return false;
+        cu.done = true;
+        return unit_segment<kSparse, kSched == kSchedMerge>(p, n_items, s);
+    }
+}
+
+// kSched: see the schedules above (kSchedMerge carries the in-kernel merge code,
+// kept out of the plain variant: small launches run every path cold).
+template <bool kSparse, int kSched>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
 mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant__ CUtensorMap map_lat,
                   const __grid_constant__ CUtensorMap map_rope) {
+    constexpr bool kPersistent = kSched == kSchedPersistent;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kOffCtrl);
@@ -209,50 +368,24 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t peer = c ^ 1u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // ---- work unit: (work item, split of it, splits of it) ----
-    // Regular: one unit per (item, blockIdx.y).  With k = *tail_k > 0 the whole
-    // items come first, then the first parts of the last k items, then their
-    // second parts; tail_j numbers a cut item among the k.
+    const int pair = blockIdx.x >> 1;
     grid_dependency_wait();     // the prep (and slot check) kernels' work list and metadata
     grid_launch_dependents();
     const int n_items = __ldg(p.item_count);
-    int item_slot = blockIdx.x >> 1, split = blockIdx.y + p.split_base, nsplit = p.num_splits, share = p.split_share;
-    int tail_j = -1;
-    if (p.tail_k != nullptr) {
-        const int k = min(min(__ldg(p.tail_k), p.tail_cap), n_items), whole = n_items - k;
-        if (k > 0 && item_slot >= whole) {
-            const int j = item_slot - whole;
-            if (j >= 2 * k) return;
-            tail_j = j % k;
-            item_slot = whole + tail_j;
-            split = j / k;
-            nsplit = 2;
-            share = p.tail_share;
-        }
-    }
 
-    // ---- work item (identical in both CTAs of the pair) ----
-    if (item_slot >= n_items) return;
-    const int2 item = p.items[item_slot];
-    const int b = item.x;
-    const int tile = item.y;
-    const int T = __ldg(p.n_tree + b);
-    const int L = __ldg(p.seq_lens + b);
-    const int P = L - T;
-    const int qbase = __ldg(p.q_off + b) + kTokensPerTile * tile;
-    const int ntok = min(kTokensPerTile, T - kTokensPerTile * tile);
-    const bool bad = __ldg(p.req_state + b) != 0;
-    int nA = 0, nB = 0;
-    if constexpr (kSparse) {
-        nA = (p.topk + kBlockN - 1) / kBlockN;
-        nB = ntok > 1 ? nA : 0;
+    // ---- the first segment (identical in both CTAs of the pair) ----
+    // Every role walks the segments with its own copy of the cursor, which
+    // points past the first segment from here on.
+    Cursor cu0{};
+    if constexpr (kPersistent) {
+        cu0.x = __ldg(p.pair_begin + pair);
+        cu0.end = __ldg(p.pair_begin + pair + 1);
+        cu0.item = __ldg(p.pair_item + pair);
+        cu0.rounds = min(__ldg(p.rounds), n_items / max(p.pairs, 1));
+        cu0.pair = pair;
     }
-    const int n_kv_tiles =
-        bad ? 0 : (kSparse ? nA + nB + (T + kBlockN - 1) / kBlockN : (L + kBlockN - 1) / kBlockN);
-    int t0, t1;
-    split_range(n_kv_tiles, split, nsplit, share, t0, t1);
-    const bool merge2 = kMerge && p.merge_cnt != nullptr && nsplit == 2;
-    const int n = t1 - t0;
+    Seg seg0;
+    if (!next_segment<kSparse, kSched>(p, n_items, cu0, seg0)) return;
 
     // rows of this thread (softmax warps only)
     const int q4 = warp & 3;
@@ -260,27 +393,29 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int tok_local = r / kHeads;
     const int head = r % kHeads;
     const bool softmax_warp = warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4;
-    const bool row_valid = softmax_warp && tok_local < ntok;
-    const int qidx = qbase + tok_local;
-    const long long grow = static_cast<long long>(qidx) * kHeads + head;  // global output row
-
-    // ---- two-split merge (softmax warps) ----
-    // With exactly two KV splits the two work units of a row tile meet per CTA
-    // half c: the first to arrive writes its normalised partial and lse and
-    // marks them written; the second waits for the mark, copies the other
-    // split's rows of its half into shared memory in one batch of async copies
-    // (the stages, q rope and receive buffer are free by then), and writes the
-    // merged rows, weighting the splits by their lse and adding them in split
-    // order, so the result does not depend on which unit arrives second.  Rows
-    // leave through the warp's 4 KB tile of the P buffers in whole 128-byte
-    // lines.  own(part, v) fills v[32] with this unit's normalised columns
-    // 32 part .. 32 part + 31 of the thread's row; lse_own is its lse.
     const long long out_rows = static_cast<long long>(p.total_q) * kHeads;
-    // rows of this tile in the partial buffers: its global rows, or the cut item's compact slot
-    const long long part_row0 = tail_j >= 0 ? static_cast<long long>(tail_j) * kRows : static_cast<long long>(qbase) * kHeads;
-    const long long part_rows = tail_j >= 0 ? static_cast<long long>(p.tail_cap) * kRows : out_rows;
-    auto two_split_merge = [&](auto&& own, float lse_own) {
-        int32_t* cnt = p.merge_cnt + (item_slot * 2 + static_cast<int>(c)) * 2;
+
+    // ---- two-split merge (per-unit grid; softmax warps) ----
+    // With exactly two KV splits (or a cut unit) the two work units of a row
+    // tile meet per CTA half c: the first to arrive writes its normalised
+    // partial and lse and marks them written; the second waits for the mark,
+    // copies the other split's rows of its half into shared memory in one batch
+    // of async copies (the stages, q rope and receive buffer are free by then:
+    // a unit is the CTA's only segment), and writes the merged rows, weighting
+    // the splits by their lse and adding them in split order, so the result
+    // does not depend on which unit arrives second.  Rows leave through the
+    // warp's 4 KB tile of the P buffers in whole 128-byte lines.  own(part, v)
+    // fills v[32] with this unit's normalised columns 32 part .. 32 part + 31 of
+    // the thread's row; lse_own is its lse.
+    auto two_split_merge = [&](const Seg& sg, auto&& own, float lse_own) {
+        const bool row_valid = tok_local < sg.ntok;
+        const long long grow = static_cast<long long>(sg.qbase + tok_local) * kHeads + head;
+        // rows of this tile in the partial buffers: its global rows, or the cut item's compact slot
+        const long long part_row0 =
+            sg.tail_j >= 0 ? static_cast<long long>(sg.tail_j) * kRows : static_cast<long long>(sg.qbase) * kHeads;
+        const long long part_rows = sg.tail_j >= 0 ? static_cast<long long>(p.tail_cap) * kRows : out_rows;
+        const int split = sg.split;
+        int32_t* cnt = p.merge_cnt + (sg.item * 2 + static_cast<int>(c)) * 2;
         float* lse2 = p.part_lse + static_cast<long long>(c) * 2 * part_rows;   // [half][split][row]
         const long long prow = part_row0 + r, pwrow = part_row0 + q4 * 32;   // this row / the warp's first
         const uint32_t ebuf = smem_u32(smem + kOffP) + q4 * 4096;
@@ -312,7 +447,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (row_valid) lse2[split * part_rows + prow] = lse_own;
             __threadfence();
             named_bar_sync(4, kSoftmaxThreads);
-            const bool skip_mark = fault_kind() == 2 && item_slot == 0 && c == 0;
+            const bool skip_mark = fault_kind() == 2 && sg.item == 0 && c == 0;
             if (r == 0 && !skip_mark) atomicExch(cnt + 1, 1);
             return;
         }
@@ -388,64 +523,66 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         if (row_valid && c == 0) p.lse[grow] = lse_tot;
     };
 
-    if (n <= 0) {
-        // Empty split or invalid request: normalised output 0, lse -inf.
-        if (merge2) {
-            if (softmax_warp)
-                two_split_merge([](int, float* v) {
+    if constexpr (!kPersistent) {
+        if (seg0.n <= 0) {
+            // Empty split or invalid request: normalised output 0, lse -inf.
+            if (seg0.kind == kOutTwoSplit) {
+                if (softmax_warp)
+                    two_split_merge(seg0, [](int, float* v) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = 0.f;
-                }, -INFINITY);
+                        for (int k = 0; k < 32; ++k) v[k] = 0.f;
+                    }, -INFINITY);
+                return;
+            }
+            if (softmax_warp && tok_local < seg0.ntok) {
+                const long long grow = static_cast<long long>(seg0.qbase + tok_local) * kHeads + head;
+                const long long slot_row = static_cast<long long>(seg0.split - p.split_base) * out_rows + grow;
+                float* dst = seg0.kind == kOutFinal ? p.out + grow * kDLatent + kDLatentHalf * c
+                                                    : p.part_out + slot_row * kDLatent + kDLatentHalf * c;
+                for (int d = 0; d < kDLatentHalf; d += 4)
+                    *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c == 0) {
+                    if (seg0.kind == kOutFinal) p.lse[grow] = -INFINITY;
+                    else p.part_lse[slot_row] = -INFINITY;
+                }
+            }
             return;
         }
-        if (row_valid) {
-            float* dst = (nsplit == 1)
-                             ? p.out + grow * kDLatent + kDLatentHalf * c
-                             : p.part_out + (static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow) *
-                                       kDLatent + kDLatentHalf * c;
-            for (int d = 0; d < kDLatentHalf; d += 4)
-                *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c == 0) {
-                if (nsplit == 1) p.lse[grow] = -INFINITY;
-                else p.part_lse[static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow] = -INFINITY;
-            }
-        }
-        return;
     }
 
     // Sparse gather warps: lane l of warp h handles key 32h + l of every tile.
-    // The slot values of the first tiles are loaded before the set-up below.
+    // The slot values of the first segment's first tiles are loaded before the set-up below.
     [[maybe_unused]] const int half = warp == 0 ? 0 : 1;
     [[maybe_unused]] const int key = 32 * half + lane;
-    // raw slot value of this lane's key in local tile jj (a KV position, -1 for none)
-    [[maybe_unused]] auto slot_raw = [&](int jj) -> int {
-        if (jj >= n) return -1;
+    // raw slot value of this lane's key in local tile jj of segment sg (a KV position, -1 for none)
+    [[maybe_unused]] auto slot_raw = [&](const Seg& sg, int jj) -> int {
+        if (jj >= sg.n) return -1;
         int kind, base;
-        sparse_segment(t0 + jj, nA, nB, kind, base);
-        if (kind == 2) return base + key < T ? P + base + key : -1;
+        sparse_segment(sg.t0 + jj, sg.nA, sg.nB, kind, base);
+        if (kind == 2) return base + key < sg.T ? sg.P + base + key : -1;
         return base + key < p.topk
-                   ? __ldg(p.topk_idx + static_cast<long long>(qbase + kind) * p.topk + base + key)
+                   ? __ldg(p.topk_idx + static_cast<long long>(sg.qbase + kind) * p.topk + base + key)
                    : -1;
     };
     [[maybe_unused]] int pre_raw[3] = {-1, -1, -1};
     if constexpr (kSparse) {
         if (warp == 0 || warp == kGatherWarp2) {
 #pragma unroll
-            for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(t);
+            for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(seg0, t);
         }
     }
 
-    // Softmax warps: the query copies (global -> shared, into the staging and P
-    // buffers, which nothing uses yet); the rows move into TMEM after the
-    // set-up.  Each warp copies its 32 rows, one whole 512-byte row half per
+    // Softmax warps: the query copies of a segment (global -> shared, into the
+    // staging and P buffers, which nothing uses then); the rows move into TMEM
+    // afterwards.  Each warp copies its 32 rows, one whole 512-byte row half per
     // instruction (unit u of row i at u ^ i), the rope half straight into its
-    // swizzled slot.  The dense kernel starts them before the set-up; the
-    // sparse one after it, so that they do not delay the first tile's slot and
-    // block-table lookups, which gate its first QK.
-    auto issue_q_copies = [&]() {
+    // swizzled slot.  The dense kernel starts the first segment's copies before
+    // the set-up; the sparse one after it, so that they do not delay the first
+    // tile's slot and block-table lookups, which gate its first QK.
+    auto issue_q_copies = [&](const Seg& sg) {
         const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;
         const uint32_t qrope = smem_u32(smem + kOffQRope);
-        const long long row0 = static_cast<long long>(qbase) * kHeads + q4 * 32;
+        const long long row0 = static_cast<long long>(sg.qbase) * kHeads + q4 * 32;
         const uint8_t* lat = reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2;
 #pragma unroll 8
         for (int i = 0; i < 32; ++i)
@@ -459,7 +596,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         }
         cp_async_commit();
     };
-    if (!kSparse && softmax_warp && row_valid) issue_q_copies();
+    if (!kSparse && softmax_warp && tok_local < seg0.ntok && seg0.n > 0) issue_q_copies(seg0);
 
     // ---- set-up ----
     if (threadIdx.x == 0) {
@@ -505,6 +642,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
     const uint32_t p_addr = smem_u32(smem + kOffP);
 
+    // The roles below walk the same segments; tile i of the CTA's whole stream
+    // (all segments) uses KV stage i % kStages, S buffer and P barriers i & 1.
     if (warp == 0 || (kSparse && warp == kGatherWarp2)) {
         // ================= TMA producer(s) =================
         // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: warps 0
@@ -521,125 +660,137 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // loaded; each loaded value is first used one tile later.
         const uint64_t policy = l2_policy_evict_last();
         bool ok = true;
-        int issued = 0;
-        // checked position of a raw slot value of tile jt (slot positions the check
-        // kernel rejected, >= P, are dropped); its block-table load is issued, not waited on
-        [[maybe_unused]] auto translate = [&](int jt, int raw, int& tpos, int& page) {
-            int kind, base;
-            sparse_segment(t0 + jt, nA, nB, kind, base);
-            tpos = (raw < 0 || (kind != 2 && raw >= P)) ? -1 : raw;
-            page = tpos >= 0 ? __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + tpos / p.page_size)
-                             : -1;
-        };
-        // cache row from a checked position and its (landed) block-table entry
-        [[maybe_unused]] auto row_of = [&](int tpos, int page) -> int {
-            if (tpos < 0) return -1;
-            if (page < 0 || page >= p.num_pages) {
-                raise_status(p.status, kStatusBadBlock);
-                return -1;
-            }
-            return page * p.page_size + tpos % p.page_size;
-        };
-        // this CTA's 576 bytes of a row span five 128-byte lines
-        [[maybe_unused]] auto prefetch_row = [&](int row) {
-            if (row < 0) return;
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.kv) + static_cast<long long>(row) * (kDqk * 2);
+        int issued = 0;   // tiles issued into the ring
+        Cursor cu = cu0;
+        Seg sg = seg0;
+        for (bool have = true, first = true; have && ok;
+             have = next_segment<kSparse, kSched>(p, n_items, cu, sg), first = false) {
+            const int n = sg.n;
+            if (n <= 0) continue;
+            // checked position of a raw slot value of tile jt (slot positions the check
+            // kernel rejected, >= P, are dropped); its block-table load is issued, not waited on
+            [[maybe_unused]] auto translate = [&](int jt, int raw, int& tpos, int& page) {
+                int kind, base;
+                sparse_segment(sg.t0 + jt, sg.nA, sg.nB, kind, base);
+                tpos = (raw < 0 || (kind != 2 && raw >= sg.P)) ? -1 : raw;
+                page = tpos >= 0 ? __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages + tpos / p.page_size)
+                                 : -1;
+            };
+            // cache row from a checked position and its (landed) block-table entry
+            [[maybe_unused]] auto row_of = [&](int tpos, int page) -> int {
+                if (tpos < 0) return -1;
+                if (page < 0 || page >= p.num_pages) {
+                    raise_status(p.status, kStatusBadBlock);
+                    return -1;
+                }
+                return page * p.page_size + tpos % p.page_size;
+            };
+            // this CTA's 576 bytes of a row span five 128-byte lines
+            [[maybe_unused]] auto prefetch_row = [&](int row) {
+                if (row < 0) return;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(p.kv) + static_cast<long long>(row) * (kDqk * 2);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) prefetch_l2(src + kDLatentHalf * 2 * c + 128 * ch);
-            prefetch_l2(src + kDLatent * 2 + kDRopeHalf * 2 * c);
-        };
-        [[maybe_unused]] int raw = -1;   // slot value (tile jj + 3)
-        [[maybe_unused]] int tpos = -1;  // checked position (tile jj + 2) ...
-        [[maybe_unused]] int page = -1;  // ... and its block-table entry, in flight
-        [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
-        [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
-        [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
-        if constexpr (kSparse) {
-            // slot values of tiles 0..2 were loaded before the set-up; the
-            // block-table entries of tiles 0 and 1 are one more round trip
-            raw = pre_raw[2];
-            int tpos0, page0;
-            translate(0, pre_raw[0], tpos0, page0);
-            translate(1, pre_raw[1], tpos, page);
-            cur = row_of(tpos0, page0);
-            prefetch_row(cur);
-        }
-        for (int jj = 0; jj < n && ok; ++jj) {
-            const int st = jj % kStages;
+                for (int ch = 0; ch < 4; ++ch) prefetch_l2(src + kDLatentHalf * 2 * c + 128 * ch);
+                prefetch_l2(src + kDLatent * 2 + kDRopeHalf * 2 * c);
+            };
+            [[maybe_unused]] int raw = -1;   // slot value (tile jj + 3)
+            [[maybe_unused]] int tpos = -1;  // checked position (tile jj + 2) ...
+            [[maybe_unused]] int page = -1;  // ... and its block-table entry, in flight
+            [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
+            [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
+            [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
             if constexpr (kSparse) {
-                if (jj + 1 < n) {
-                    nxt = row_of(tpos, page);
-                    prefetch_row(nxt);
-                }
-                if (jj + 2 < n) {
-                    translate(jj + 2, raw, tpos, page);
-                    raw = slot_raw(jj + 3);
-                }
-            }
-            if (jj >= kStages) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((jj / kStages) - 1) & 1, abort_flag, lim));
-                if (!ok) break;
-            }
-            uint8_t* dst = smem + kOffStages + st * kStageBytes;
-            if constexpr (kSparse) {
-                const uint32_t mask = __ballot_sync(0xffffffffu, cur >= 0);
-                int y[4];
+                // the first segment's slot values of tiles 0..2 were loaded before the
+                // set-up; the block-table entries of tiles 0 and 1 are one more round trip
+                if (!first) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int v = __shfl_sync(0xffffffffu, cur, (4 * lane + t) & 31);
-                    y[t] = v >= 0 ? v : oob_row;
+                    for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(sg, t);
                 }
-                if (lane == 0) {
-                    ctl->slot_mask[st][half] = mask;
-                    mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes / 2);  // releases the mask with the tile
-                }
-                __syncwarp();
-                if (lane < 8) {
-                    const int g = 8 * half + lane;  // keys 4g .. 4g + 3
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-                        tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
-                                    kDLatentHalf * static_cast<int>(c) + 64 * ch, y[0], y[1], y[2], y[3], policy);
-                    tma_gather4(dst + 4 * kChunkBytes + 4 * g * 64, &map_rope, &ctl->kv_full[st],
-                                kDLatent + kDRopeHalf * static_cast<int>(c), y[0], y[1], y[2], y[3], policy);
-                }
-                cur = nxt;
-                ++issued;
-                __syncwarp();
-            } else {
-                const int kpos = (t0 + jj) * kBlockN;
-                if (lane == 0) {
-                    const int page_idx = kpos / p.page_size;
-                    const int page = __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + page_idx);
-                    if (page < 0 || page >= p.num_pages) raise_status(p.status, kStatusBadBlock);
-                    // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
-                    const int row = page * p.page_size + (kpos % p.page_size);
-                    mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
-                    for (int ch = 0; ch < 4; ++ch)
-                        tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
-                                    kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
-                    tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
-                                kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
-                }
-                ++issued;
-                __syncwarp();
-                if (kpos + kBlockN > L) {
-                    // Last, partial tile: zero the rows past seq_len so that masked
-                    // keys multiply finite values in PV.
-                    ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim));
-                    if (!ok) break;
-                    const int kvalid = L - kpos;
-                    uint8_t* base = smem + kOffStages + st * kStageBytes;
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
-                        const int u = lane % 8;  // 16-byte unit of the row
-                        for (int ch = 0; ch < 4; ++ch)
-                            *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
-                        if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                raw = pre_raw[2];
+                int tpos0, page0;
+                translate(0, pre_raw[0], tpos0, page0);
+                translate(1, pre_raw[1], tpos, page);
+                cur = row_of(tpos0, page0);
+                prefetch_row(cur);
+            }
+            for (int jj = 0; jj < n && ok; ++jj) {
+                const int gi = issued;
+                const int st = gi % kStages;
+                if constexpr (kSparse) {
+                    if (jj + 1 < n) {
+                        nxt = row_of(tpos, page);
+                        prefetch_row(nxt);
                     }
-                    fence_proxy_async_smem();
+                    if (jj + 2 < n) {
+                        translate(jj + 2, raw, tpos, page);
+                        raw = slot_raw(sg, jj + 3);
+                    }
+                }
+                if (gi >= kStages) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((gi / kStages) - 1) & 1, abort_flag, lim));
+                    if (!ok) break;
+                }
+                uint8_t* dst = smem + kOffStages + st * kStageBytes;
+                if constexpr (kSparse) {
+                    const uint32_t mask = __ballot_sync(0xffffffffu, cur >= 0);
+                    int y[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int v = __shfl_sync(0xffffffffu, cur, (4 * lane + t) & 31);
+                        y[t] = v >= 0 ? v : oob_row;
+                    }
+                    if (lane == 0) {
+                        ctl->slot_mask[st][half] = mask;
+                        mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes / 2);  // releases the mask with the tile
+                    }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                    if (lane < 8) {
+                        const int g = 8 * half + lane;  // keys 4g .. 4g + 3
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
+                                        kDLatentHalf * static_cast<int>(c) + 64 * ch, y[0], y[1], y[2], y[3], policy);
+                        tma_gather4(dst + 4 * kChunkBytes + 4 * g * 64, &map_rope, &ctl->kv_full[st],
+                                    kDLatent + kDRopeHalf * static_cast<int>(c), y[0], y[1], y[2], y[3], policy);
+                    }
+                    cur = nxt;
+                    ++issued;
+                    __syncwarp();
+                } else {
+                    const int kpos = (sg.t0 + jj) * kBlockN;
+                    if (lane == 0) {
+                        const int page_idx = kpos / p.page_size;
+                        const int pg = __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages + page_idx);
+                        if (pg < 0 || pg >= p.num_pages) raise_status(p.status, kStatusBadBlock);
+                        // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
+                        const int row = pg * p.page_size + (kpos % p.page_size);
+                        mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
+                        for (int ch = 0; ch < 4; ++ch)
+                            tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
+                                        kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
+                        tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
+                                    kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
+                    }
+                    ++issued;
+                    __syncwarp();
+                    if (kpos + kBlockN > sg.L) {
+                        // Last, partial tile: zero the rows past seq_len so that masked
+                        // keys multiply finite values in PV.
+                        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim));
+                        if (!ok) break;
+                        const int kvalid = sg.L - kpos;
+                        uint8_t* base = smem + kOffStages + st * kStageBytes;
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
+                            const int u = lane % 8;  // 16-byte unit of the row
+                            for (int ch = 0; ch < 4; ++ch)
+                                *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
+                            if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                    }
                 }
             }
         }
@@ -657,37 +808,56 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // ================= QK issuer =================
         const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
         const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, 0, abort_flag, lim));
-        tc_fence_after();
-        for (int jj = 0; jj < n && ok; ++jj) {
-            const int st = jj % kStages;
-            const int x = jj & 1;
-            const bool tail = !kSparse && (t0 + jj) * kBlockN + kBlockN > L;
-            const bool inject = fault_kind() == 1 && item_slot == 0 && split == 0 && c == 0 && jj == 1;
-            ok = inject ? mbar_wait(&ctl->never, 0, abort_flag, lim)
-                 : tail ? mbar_wait(&ctl->kv_fixed[st], 0, abort_flag, lim)
-                        : mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
-            // S buffer x held tile jj - 2; the softmax threads have read it out
-            if (ok && jj >= 2) ok = mbar_wait(&ctl->s_free[x], ((jj - 2) >> 1) & 1, abort_flag, lim);
-            ok = __all_sync(0xffffffffu, ok);
+        bool ok = true;
+        int g = 0;              // tiles of the earlier segments
+        int segs = 0;           // segments with tiles so far (phases of q_ready)
+        uint32_t fixpar = 0;    // bit st: parity of the next phase of kv_fixed[st]
+        Cursor cu = cu0;
+        Seg sg = seg0;
+        for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
+            const int n = sg.n;
+            if (n <= 0) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, segs & 1, abort_flag, lim));
+            ++segs;
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-                const uint32_t sb = stage0 + st * kStageBytes;
-                const uint32_t dS = tmem + kTmS + 64 * x;
-                // one base descriptor per operand; the k-steps add constant byte offsets
-                const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
-                const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
+            for (int jj = 0; jj < n; ++jj) {
+                const int gi = g + jj;
+                const int st = gi % kStages;
+                const int x = gi & 1;
+                const bool tail = !kSparse && (sg.t0 + jj) * kBlockN + kBlockN > sg.L;
+                const bool inject = fault_kind() == 1 && sg.item == 0 && sg.split == 0 && c == 0 && jj == 1;
+                if (inject) {
+                    ok = mbar_wait(&ctl->never, 0, abort_flag, lim);
+                } else if (tail) {
+                    ok = mbar_wait(&ctl->kv_fixed[st], (fixpar >> st) & 1u, abort_flag, lim);
+                    fixpar ^= 1u << st;
+                } else {
+                    ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
+                }
+                // S buffer x held tile gi - 2; the softmax threads have read it out
+                if (ok && gi >= 2) ok = mbar_wait(&ctl->s_free[x], ((gi - 2) >> 1) & 1, abort_flag, lim);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sb = stage0 + st * kStageBytes;
+                    const uint32_t dS = tmem + kTmS + 64 * x;
+                    // one base descriptor per operand; the k-steps add constant byte offsets
+                    const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
+                    const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
 #pragma unroll
-                for (int k = 0; k < kDLatentHalf / 16; ++k)
-                    mma_ts(dS, tmem + kTmQ + 8 * k, desc_advance(bk, (k >> 2) * kChunkBytes + (k & 3) * 32),
-                           idesc_qk, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < kDLatentHalf / 16; ++k)
+                        mma_ts(dS, tmem + kTmQ + 8 * k, desc_advance(bk, (k >> 2) * kChunkBytes + (k & 3) * 32),
+                               idesc_qk, k > 0 ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < kDRopeHalf / 16; ++k)
-                    mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
-                mma_commit(&ctl->s_full[x]);
+                    for (int k = 0; k < kDRopeHalf / 16; ++k)
+                        mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
+                    mma_commit(&ctl->s_full[x]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            g += n;
         }
         if (!ok) {
             if (lane == 0) raise_status(p.status, kStatusTimeout);
@@ -704,28 +874,37 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint64_t ap_hi = smem_desc(p_addr, 16, 1024, kSwizzle128B);
         const uint64_t ap_lo = smem_desc(p_addr + kPBytes, 16, 1024, kSwizzle128B);
         bool ok = true;
-        for (int i = 0; i < n && ok; ++i) {
-            const int x = i & 1;
-            const int st = i % kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (i >> 1) & 1, abort_flag, lim));
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
-                const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                if (lo) {
+        int g = 0;
+        Cursor cu = cu0;
+        Seg sg = seg0;
+        for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
+            const int n = sg.n;
+            if (n <= 0) continue;
+            for (int i = 0; i < n && ok; ++i) {
+                const int gi = g + i;
+                const int x = gi & 1;
+                const int st = gi % kStages;
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (gi >> 1) & 1, abort_flag, lim));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
+                    const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                        mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    if (lo) {
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                    }
+                    mma_commit(&ctl->pv_done[x]);
+                    mma_commit(&ctl->kv_empty[st]);
                 }
-                mma_commit(&ctl->pv_done[x]);
-                mma_commit(&ctl->kv_empty[st]);
+                __syncwarp();
             }
-            __syncwarp();
+            g += n;
         }
         if (!ok) {
             if (lane == 0) raise_status(p.status, kStatusTimeout);
@@ -739,42 +918,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // ================= softmax / epilogue (thread = row) =================
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
-        // q latent half -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory.
-        // The warp's async copies land in its 16 KB slice of the staging and P
-        // buffers (nothing uses them before q_ready);
-        // then the thread of each row moves the row into TMEM.  A warp's rows
-        // belong to one token, so row_valid is warp-uniform; rows of a missing
-        // second token are zeros.
-        {
-            const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;
-            if (row_valid) {
-                if constexpr (kSparse) issue_q_copies();
-                cp_async_wait<0>();
-            } else {
-                for (int u = 0; u < 4; ++u)
-                    st_shared_v4(qrope_addr + r * 64 + ((u ^ ((r >> 1) & 3)) << 4), 0.f, 0.f, 0.f, 0.f);
-            }
-            __syncwarp();
-            for (int part = 0; part < 4; ++part) {
-                uint32_t v[32];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float4 w = row_valid ? ld_shared_v4(qbuf + lane * 512 + (((8 * part + u) ^ lane) << 4))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[4 * u + 0] = __float_as_uint(w.x);
-                    v[4 * u + 1] = __float_as_uint(w.y);
-                    v[4 * u + 2] = __float_as_uint(w.z);
-                    v[4 * u + 3] = __float_as_uint(w.w);
-                }
-                tmem_st32(trow + kTmQ + 32 * part, v);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&ctl->q_ready);
-        }
-
-        const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
         const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
         const uint32_t xbuf_peer = mapa(xbuf_local, peer);
         const uint32_t stg_local = smem_u32(smem + kOffStaging);
@@ -782,14 +925,18 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t rowbase = stg_local + r * (kBlockN * 4);       // this row in the staging buffer
         const uint32_t peerbase = xbuf_local + r * (kBlockN * 4);     // this row in the receive buffer
         const uint32_t prow = p_addr + r * 128;                       // this row of P (128 bytes)
+        const uint32_t qbuf = stg_local + q4 * 16384;                 // this warp's 16 KB of the staging + P region
+        const uint32_t ebuf = p_addr + q4 * 4096;                     // this warp's 4 KB output tile
         int posted = 1;    // incoming partials whose byte count is posted (thread r == 0)
         int consumed = 0;  // incoming partials waited for (thread r == 0)
-        float m_use = -INFINITY;
-        float l = 0.f;
         bool ok = true;
+        int g = 0;         // tiles of the earlier segments (sent and received partials)
+        Cursor cu = cu0;
+        Seg sg = seg0;
 
-        // Step C of tile t: partial scores TMEM -> staging -> the peer's receive buffer.
-        // Every softmax thread takes part in the named barrier, whatever its `ok`.
+        // Step C of tile t (of the CTA's stream): partial scores TMEM -> staging ->
+        // the peer's receive buffer.  Every softmax thread takes part in the named
+        // barrier, whatever its `ok`.
         auto stage_and_send = [&](int t) {
             const int x = t & 1;
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&ctl->s_full[x], (t >> 1) & 1, abort_flag, lim));
@@ -798,13 +945,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int hh = 0; hh < 2; ++hh) {
                     uint32_t a[32];
-                    tmem_ld32(trow + kTmS + 64 * x + 32 * half, a);
+                    tmem_ld32(trow + kTmS + 64 * x + 32 * hh, a);
                     tmem_wait_ld();
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const int uu = 8 * half + u;
+                        const int uu = 8 * hh + u;
                         st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
                                      __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
                                      __uint_as_float(a[4 * u + 3]));
@@ -818,184 +965,494 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (r == 0 && ok) {
                 // the peer has read the partial this CTA sent before (its receive buffer is free)
                 if (t >= 1) ok = mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
-                const bool skip_send = fault_kind() == 3 && item_slot == 0 && split == 0 && c == 0 && t == 1;
+                const bool skip_send = fault_kind() == 3 && sg.item == 0 && sg.split == 0 && c == 0 && t == 1;
                 if (ok && !skip_send) bulk_copy_to_peer(xbuf_peer, stg_local, kXBufBytes, xfull_peer);
             }
         };
 
-        if (n > 0) stage_and_send(0);
-        for (int jj = 0; jj < n; ++jj) {
-            const int x = jj & 1;
-            // ---- A/B: full scores = own partial (staging) + the peer's (receive buffer) ----
-            if (ok) ok = mbar_wait<true>(&ctl->x_full, jj & 1, abort_flag, lim);
-            float s[kBlockN];
-            if (ok) {
-                if (r == 0) {
-                    ++consumed;
-                    mbar_arrive_remote_relaxed(&ctl->stg_free, peer);  // our staging landed: peer may reuse its own
-                }
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const uint32_t sw = (u ^ (r & 7)) << 4;
-                    const float4 a = ld_shared_v4(rowbase + sw);
-                    const float4 v = ld_shared_v4(peerbase + sw);
-                    s[4 * u] = a.x + v.x;
-                    s[4 * u + 1] = a.y + v.y;
-                    s[4 * u + 2] = a.z + v.z;
-                    s[4 * u + 3] = a.w + v.w;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
+        // ---- persistent: merge of an item cut between CTA pairs ----
+        // The pieces of item sg.item are the non-empty shares of pairs q_first,
+        // q_first + 1, ... that start before the item's end; piece of pair q has
+        // partial slot 2q (the first segment of the pair) or 2q + 1 (its last).
+        // Per CTA half, the first pieces to finish write their normalised partial
+        // and lse and count themselves written; the last to arrive waits for the
+        // others, then sums w_k * o_k over the pieces in piece order (w_k from
+        // the lse of all pieces) into TMEM columns [256, 512), free in an
+        // epilogue, reading the other pieces' rows through the staging and P
+        // buffers (16 KB per warp, half a row at a time), and writes the rows.
+        // own(part, v): this piece's normalised columns; sent: partials this CTA
+        // has shipped so far (the staging buffer is reused once the last landed).
+        // Every term is rounded the same way whichever piece merges (explicit
+        // fused multiply-adds), so the result does not depend on arrival order.
+        auto piece_merge = [&](auto&& own, float lse_own, int sent) {
+            const bool row_valid = tok_local < sg.ntok;
+            const long long grow = static_cast<long long>(sg.qbase + tok_local) * kHeads + head;
+            const long long O = __ldg(p.woff + sg.item), E = __ldg(p.woff + sg.item + 1);
+            const int q_first = __ldg(p.item_first_pair + sg.item);
+            int np = 0;
+            for (int q = q_first; q < p.pairs; ++q) {
+                const long long b0 = __ldg(p.pair_begin + q);
+                if (b0 >= E) break;
+                np += __ldg(p.pair_begin + q + 1) > b0 ? 1 : 0;
             }
-            // the receive buffer has been read by all 128 threads: let the peer send the next tile
-            named_bar_sync(2, kSoftmaxThreads);
-            if (r == 0 && ok) {
-                if (jj + 1 < n) {
-                    mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
-                    ++posted;
-                }
-                mbar_arrive_remote_relaxed(&ctl->x_empty, peer);
-            }
-            // ---- C: ship the next tile's partial scores; its copy overlaps this tile's math ----
-            if (jj + 1 < n) stage_and_send(jj + 1);
-            // ---- D: this tile's softmax ----
-            // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
-            // the scale is positive, so the row max can be taken on raw scores and the scale
-            // folded into the exponent's FMA below.
-            if constexpr (kSparse) {
-                int kind, base;
-                sparse_segment(t0 + jj, nA, nB, kind, base);
-                uint64_t vis;
-                if (kind == 2) {
-                    vis = base == 0 ? anc : 0ull;  // at most 64 tree tokens: one tree tile
-                } else {
-                    // the slot mask was written before the stage was released to QK
-                    const int st = jj % kStages;
-                    if (ok) ok = mbar_wait(&ctl->kv_full[st], (jj / kStages) & 1, abort_flag, lim);
-                    const volatile uint32_t* sm = ctl->slot_mask[st];
-                    vis = kind == tok_local ? (static_cast<uint64_t>(sm[1]) << 32) | sm[0] : 0ull;
-                }
-#pragma unroll
-                for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;
-            } else {
-                const int kpos = (t0 + jj) * kBlockN;
-                if (kpos + kBlockN > P) {
-#pragma unroll
-                    for (int k = 0; k < kBlockN; ++k) {
-                        const int t = kpos + k;
-                        bool vis = t < P;
-                        if (!vis && t < L) vis = (anc >> (t - P)) & 1ull;
-                        s[k] = vis ? s[k] : -INFINITY;
-                    }
-                }
-            }
-            // tree reductions (8 independent chains) keep the dependent latency short
-            float mx[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = s[k];
-#pragma unroll
-            for (int k = 8; k < kBlockN; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
-            const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;  // log2 units
-            // ---- lazy online-softmax rescale (warp-uniform TMEM traffic) ----
-            const bool grow_max = ok && mt > m_use + kLazyRescaleLog2;
-            float alpha = 1.f;
-            if (grow_max) {
-                alpha = ex2_approx(m_use - mt);  // 0 when m_use is -inf
-                m_use = mt;
-                l *= alpha;
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            // PV of the previous tile must be done before O is rescaled and before its
-            // P buffer is overwritten (it normally finished long ago)
-            if (ok && jj > 0)
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1,
-                                                       abort_flag, lim));
-            if (ok && jj > 0 && __any_sync(0xffffffffu, grow_max)) {
-                tc_fence_after();
+            auto slot_of = [&](int q) { return 2 * q + (__ldg(p.pair_begin + q) >= O ? 0 : 1); };
+            int32_t* cnt = p.merge_cnt + (sg.item * 2 + static_cast<int>(c)) * 2;
+            named_bar_sync(4, kSoftmaxThreads);
+            if (r == 0) ctl->merge_role = atomicAdd(cnt, 1);
+            named_bar_sync(4, kSoftmaxThreads);
+            const int role = *reinterpret_cast<volatile int*>(&ctl->merge_role);
+            if (role < np - 1) {
+                const int slot = slot_of(pair);
+                float* wdst = p.part_out + (static_cast<long long>(slot) * kRows + q4 * 32) * kDLatent + kDLatentHalf * c;
                 for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                    float v[32];
+                    own(part, v);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), v[4 * u], v[4 * u + 1],
+                                     v[4 * u + 2], v[4 * u + 3]);
+                    __syncwarp();
+                    if (row_valid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int row = 4 * i + (lane >> 3), u = lane & 7;
+                            *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) =
+                                ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (row_valid) p.part_lse[(static_cast<long long>(slot) * 2 + c) * kRows + r] = lse_own;
+                __threadfence();
+                named_bar_sync(4, kSoftmaxThreads);
+                const bool skip_mark = fault_kind() == 4 && c == 0;
+                if (r == 0 && !skip_mark) atomicAdd(cnt + 1, 1);
+                return;
+            }
+            if (r == 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (atomicAdd(cnt + 1, 0) < np - 1) {
+                    if (globaltimer_ns() - t0 > p.timeout_ns) {
+                        raise_status(p.status, kStatusTimeout);
+                        break;
+                    }
+                    __nanosleep(100);
+                }
+            }
+            named_bar_sync(4, kSoftmaxThreads);
+            __threadfence();
+            // lse of the merged row: log-sum-exp over the pieces' lse
+            auto lse_of = [&](int q) -> float {
+                if (q == pair) return lse_own;
+                return row_valid ? __ldcg(p.part_lse + (static_cast<long long>(slot_of(q)) * 2 + c) * kRows + r)
+                                 : -INFINITY;
+            };
+            float m = -INFINITY;
+            for (int q = q_first, k = 0; k < np; ++q) {
+                if (__ldg(p.pair_begin + q + 1) <= __ldg(p.pair_begin + q)) continue;
+                m = fmaxf(m, lse_of(q));
+                ++k;
+            }
+            float lse_tot = -INFINITY;
+            if (m != -INFINITY) {
+                float sum = 0.f;
+                for (int q = q_first, k = 0; k < np; ++q) {
+                    if (__ldg(p.pair_begin + q + 1) <= __ldg(p.pair_begin + q)) continue;
+                    const float lk = lse_of(q);
+                    sum += lk == -INFINITY ? 0.f : __expf(lk - m);
+                    ++k;
+                }
+                lse_tot = m + __logf(sum);
+            }
+            // the staging buffer is the source of this CTA's last partial-score copy until it landed
+            if (sent > 0) mbar_wait<true>(&ctl->stg_free, (sent - 1) & 1, abort_flag, lim);
+            for (int q = q_first, k = 0; k < np; ++q) {
+                if (__ldg(p.pair_begin + q + 1) <= __ldg(p.pair_begin + q)) continue;
+                const float lk = lse_of(q);
+                const float w = (lk == -INFINITY || lse_tot == -INFINITY) ? 0.f : __expf(lk - lse_tot);
+                if (row_valid) {   // warp-uniform: a warp's 32 rows belong to one token
+                    if (q == pair) {
+                        for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                            float v[32];
+                            own(part, v);
+                            uint32_t a[32];
+                            if (k > 0) {
+                                tmem_ld32(trow + kTmAcc + 32 * part, a);
+                                tmem_wait_ld();
+                            }
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                a[e] = __float_as_uint(k > 0 ? __fmaf_rn(w, v[e], __uint_as_float(a[e])) : __fmul_rn(w, v[e]));
+                            tmem_st32(trow + kTmAcc + 32 * part, a);
+                        }
+                    } else {
+                        const float* src = p.part_out + (static_cast<long long>(slot_of(q)) * kRows + q4 * 32) * kDLatent +
+                                           kDLatentHalf * c;
+                        for (int hh = 0; hh < 2; ++hh) {
+                            // 32 rows x 128 columns: unit u of row i at u ^ i
+#pragma unroll 8
+                            for (int i = 0; i < 32; ++i)
+                                cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4),
+                                            src + static_cast<long long>(i) * kDLatent + 128 * hh + 4 * lane);
+                            cp_async_commit();
+                            cp_async_wait<0>();
+                            __syncwarp();
+                            for (int pp = 0; pp < 4; ++pp) {
+                                const int part = 4 * hh + pp;
+                                uint32_t a[32];
+                                if (k > 0) {
+                                    tmem_ld32(trow + kTmAcc + 32 * part, a);
+                                    tmem_wait_ld();
+                                }
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) {
+                                    const float4 t = ld_shared_v4(qbuf + lane * 512 + (((8 * pp + u) ^ lane) << 4));
+                                    const float o4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int idx = 4 * u + e;
+                                        a[idx] = __float_as_uint(k > 0 ? __fmaf_rn(w, o4[e], __uint_as_float(a[idx]))
+                                                                       : __fmul_rn(w, o4[e]));
+                                    }
+                                }
+                                tmem_st32(trow + kTmAcc + 32 * part, a);
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    tmem_wait_st();
+                }
+                ++k;
+            }
+            // the merged rows leave through the warp's 4 KB tile in whole 128-byte lines; the
+            // tiles of warps 0..3 lie in the 16 KB slice of warp 2, which may still be reading
+            named_bar_sync(4, kSoftmaxThreads);
+            if (row_valid) {
+                float* wdst = p.out + (grow - lane) * kDLatent + kDLatentHalf * c;
+                for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                    uint32_t a[32];
+                    tmem_ld32(trow + kTmAcc + 32 * part, a);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), __uint_as_float(a[4 * u]),
+                                     __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
+                                     __uint_as_float(a[4 * u + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = 4 * i + (lane >> 3), u = lane & 7;
+                        *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) =
+                            ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                    }
+                    __syncwarp();
+                }
+                if (c == 0) p.lse[grow] = lse_tot;
+            }
+        };
+
+        for (bool have = true, first = true; have && ok;
+             have = next_segment<kSparse, kSched>(p, n_items, cu, sg), first = false) {
+            const int n = sg.n;
+            const bool row_valid = tok_local < sg.ntok;
+            const int qidx = sg.qbase + tok_local;
+            const long long grow = static_cast<long long>(qidx) * kHeads + head;  // global output row
+            float m_use = -INFINITY;
+            float l = 0.f;
+            if (n > 0) {
+                // Does a later segment of this pair have tiles?  Its first partial then
+                // follows this segment's last one, and its byte count is posted in time.
+                bool more = false;
+                if constexpr (kPersistent) {
+                    Cursor c2 = cu;
+                    Seg s2;
+                    while (next_segment<kSparse, kSched>(p, n_items, c2, s2))
+                        if (s2.n > 0) {
+                            more = true;
+                            break;
+                        }
+                }
+                // ---- q of the segment -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory ----
+                // The warp's async copies land in its 16 KB slice of the staging and P
+                // buffers; then the thread of each row moves the row into TMEM.  A
+                // warp's rows belong to one token, so row_valid is warp-uniform; rows
+                // of a missing second token are zeros.  A later segment reuses the
+                // staging buffer once this CTA's last partial-score copy has landed;
+                // the previous segment's QK and PV are complete by then.
+                if (g > 0) {
+                    const bool sok = ok && mbar_wait<true>(&ctl->stg_free, (g - 1) & 1, abort_flag, lim);
+                    ok = named_bar_and(4, kSoftmaxThreads, sok);
+                    if (!ok) break;
+                }
+                if (row_valid) {
+                    if (kSparse || !first) issue_q_copies(sg);
+                    cp_async_wait<0>();
+                } else {
+                    for (int u = 0; u < 4; ++u)
+                        st_shared_v4(qrope_addr + r * 64 + ((u ^ ((r >> 1) & 3)) << 4), 0.f, 0.f, 0.f, 0.f);
+                }
+                __syncwarp();
+                for (int part = 0; part < 4; ++part) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 w = row_valid ? ld_shared_v4(qbuf + lane * 512 + (((8 * part + u) ^ lane) << 4))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[4 * u + 0] = __float_as_uint(w.x);
+                        v[4 * u + 1] = __float_as_uint(w.y);
+                        v[4 * u + 2] = __float_as_uint(w.z);
+                        v[4 * u + 3] = __float_as_uint(w.w);
+                    }
+                    tmem_st32(trow + kTmQ + 32 * part, v);
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&ctl->q_ready);
+
+                const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
+                stage_and_send(g);
+                for (int jj = 0; jj < n; ++jj) {
+                    const int gi = g + jj;
+                    const int x = gi & 1;
+                    // ---- A/B: full scores = own partial (staging) + the peer's (receive buffer) ----
+                    if (ok) ok = mbar_wait<true>(&ctl->x_full, gi & 1, abort_flag, lim);
+                    float s[kBlockN];
+                    if (ok) {
+                        if (r == 0) {
+                            ++consumed;
+                            mbar_arrive_remote_relaxed(&ctl->stg_free, peer);  // our staging landed: peer may reuse its own
+                        }
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const uint32_t sw = (u ^ (r & 7)) << 4;
+                            const float4 a = ld_shared_v4(rowbase + sw);
+                            const float4 v = ld_shared_v4(peerbase + sw);
+                            s[4 * u] = a.x + v.x;
+                            s[4 * u + 1] = a.y + v.y;
+                            s[4 * u + 2] = a.z + v.z;
+                            s[4 * u + 3] = a.w + v.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
+                    }
+                    // the receive buffer has been read by all 128 threads: let the peer send the next tile
+                    named_bar_sync(2, kSoftmaxThreads);
+                    if (r == 0 && ok) {
+                        if (jj + 1 < n || more) {
+                            mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
+                            ++posted;
+                        }
+                        mbar_arrive_remote_relaxed(&ctl->x_empty, peer);
+                    }
+                    // ---- C: ship the next tile's partial scores; its copy overlaps this tile's math ----
+                    if (jj + 1 < n) stage_and_send(gi + 1);
+                    // ---- D: this tile's softmax ----
+                    // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
+                    // the scale is positive, so the row max can be taken on raw scores and the scale
+                    // folded into the exponent's FMA below.
+                    if constexpr (kSparse) {
+                        int kind, base;
+                        sparse_segment(sg.t0 + jj, sg.nA, sg.nB, kind, base);
+                        uint64_t vis;
+                        if (kind == 2) {
+                            vis = base == 0 ? anc : 0ull;  // at most 64 tree tokens: one tree tile
+                        } else {
+                            // the slot mask was written before the stage was released to QK
+                            const int st = gi % kStages;
+                            if (ok) ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
+                            const volatile uint32_t* sm = ctl->slot_mask[st];
+                            vis = kind == tok_local ? (static_cast<uint64_t>(sm[1]) << 32) | sm[0] : 0ull;
+                        }
+#pragma unroll
+                        for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;
+                    } else {
+                        const int kpos = (sg.t0 + jj) * kBlockN;
+                        if (kpos + kBlockN > sg.P) {
+#pragma unroll
+                            for (int k = 0; k < kBlockN; ++k) {
+                                const int t = kpos + k;
+                                bool vis = t < sg.P;
+                                if (!vis && t < sg.L) vis = (anc >> (t - sg.P)) & 1ull;
+                                s[k] = vis ? s[k] : -INFINITY;
+                            }
+                        }
+                    }
+                    // tree reductions (8 independent chains) keep the dependent latency short
+                    float mx[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx[k] = s[k];
+#pragma unroll
+                    for (int k = 8; k < kBlockN; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+                    const float mt_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    const float mt = mt_raw == -INFINITY ? -INFINITY : mt_raw * p.scale_log2;  // log2 units
+                    // ---- lazy online-softmax rescale (warp-uniform TMEM traffic) ----
+                    const bool grow_max = ok && mt > m_use + kLazyRescaleLog2;
+                    float alpha = 1.f;
+                    if (grow_max) {
+                        alpha = ex2_approx(m_use - mt);  // 0 when m_use is -inf
+                        m_use = mt;
+                        l *= alpha;
+                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                    // PV of the previous tile must be done before O is rescaled and before its
+                    // P buffer is overwritten (it normally finished long ago; the previous
+                    // segment's last PV was waited for in its epilogue)
+                    if (ok && jj > 0)
+                        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(gi - 1) & 1], ((gi - 1) >> 1) & 1,
+                                                               abort_flag, lim));
+                    if (ok && jj > 0 && __any_sync(0xffffffffu, grow_max)) {
+                        tc_fence_after();
+                        for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                            uint32_t o[32];
+                            tmem_ld32(trow + kTmO + 32 * part, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tmem_st32(trow + kTmO + 32 * part, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    // ---- probabilities: p = 2^(s * scale * log2 e - m), one FMA + ex2 each ----
+                    const bool live = m_use != -INFINITY;
+                    const float neg_m = -m_use;
+                    float ps[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < kBlockN; ++k) {
+                            s[k] = ex2_approx(fmaf(s[k], p.scale_log2, neg_m));
+                            ps[k & 7] += s[k];
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
+                    }
+                    const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                    const float pmax = live ? ex2_approx(mt - m_use) : 0.f;  // the tile's largest p
+                    // One named barrier decides, uniformly for the 128 threads, whether to stop
+                    // (bit 1) and whether this tile needs the low part of P (bit 0).
+                    volatile int* flags = &ctl->tile_flags[gi % 3];
+                    const int mine = (ok ? 0 : 2) | ((pmax > kLowPartShare * (l + psum)) ? 1 : 0);
+                    if (mine) atomicOr(const_cast<int*>(flags), mine);
+                    named_bar_sync(1, kSoftmaxThreads);
+                    const int tf = *flags;
+                    if (tf & 2) {
+                        ok = false;
+                        break;
+                    }
+                    const bool need_lo = tf & 1;
+                    if (r == 0) {
+                        ctl->tile_flags[(gi + 2) % 3] = 0;  // read by everyone before this barrier; next used by tile gi + 2
+                        ctl->lo_flag[x] = need_lo ? 1 : 0;
+                    }
+                    // ---- P -> shared memory (K-major rows of 64 keys, 128-byte swizzle) ----
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        uint4 w;
+                        w.x = pack_bf16x2(s[8 * u + 0], s[8 * u + 1]);
+                        w.y = pack_bf16x2(s[8 * u + 2], s[8 * u + 3]);
+                        w.z = pack_bf16x2(s[8 * u + 4], s[8 * u + 5]);
+                        w.w = pack_bf16x2(s[8 * u + 6], s[8 * u + 7]);
+                        const uint32_t off = (u ^ (r & 7)) << 4;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off), "r"(w.x), "r"(w.y),
+                                     "r"(w.z), "r"(w.w)
+                                     : "memory");
+                        if (need_lo) {
+                            uint4 v;
+                            v.x = pack_bf16x2(s[8 * u + 0] - bf16lo_to_f32(w.x), s[8 * u + 1] - bf16hi_to_f32(w.x));
+                            v.y = pack_bf16x2(s[8 * u + 2] - bf16lo_to_f32(w.y), s[8 * u + 3] - bf16hi_to_f32(w.y));
+                            v.z = pack_bf16x2(s[8 * u + 4] - bf16lo_to_f32(w.z), s[8 * u + 5] - bf16hi_to_f32(w.z));
+                            v.w = pack_bf16x2(s[8 * u + 6] - bf16lo_to_f32(w.w), s[8 * u + 7] - bf16hi_to_f32(w.w));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + kPBytes + off),
+                                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                         : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    // The normaliser uses the fp32 weights.  Without the low part the bf16
+                    // weights that PV sees differ from them by unbiased rounding of at most
+                    // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
+                    l += psum;
+                    mbar_arrive(&ctl->p_full[x]);
+                }
+                // ---- epilogue: the segment's last PV ----
+                if (ok) ok = mbar_wait(&ctl->pv_done[(g + n - 1) & 1], ((g + n - 1) >> 1) & 1, abort_flag, lim);
+            }
+            // one decision for all 128 softmax threads (the in-kernel merges and the next
+            // segment synchronise them)
+            if constexpr (kSched == kSchedPlain) ok = __all_sync(0xffffffffu, ok);
+            else ok = named_bar_and(4, kSoftmaxThreads, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float lse_v = (l > 0.f ? m_use + log2f(l) : -INFINITY) * 0.6931471805599453f;
+            // this segment's normalised columns 32 part .. 32 part + 31 of the thread's row
+            auto own = [&](int part, float* v) {
+                if (n > 0) {
                     uint32_t o[32];
                     tmem_ld32(trow + kTmO + 32 * part, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tmem_st32(trow + kTmO + 32 * part, o);
+                    for (int k = 0; k < 32; ++k) v[k] = __fmul_rn(__uint_as_float(o[k]), inv_l);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = 0.f;
                 }
-                tmem_wait_st();
-            }
-            // ---- probabilities: p = 2^(s * scale * log2 e - m), one FMA + ex2 each ----
-            const bool live = m_use != -INFINITY;
-            const float neg_m = -m_use;
-            float ps[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) ps[k] = 0.f;
-            if (live) {
-#pragma unroll
-                for (int k = 0; k < kBlockN; ++k) {
-                    s[k] = ex2_approx(fmaf(s[k], p.scale_log2, neg_m));
-                    ps[k & 7] += s[k];
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
-            }
-            const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            const float pmax = live ? ex2_approx(mt - m_use) : 0.f;  // the tile's largest p
-            // One named barrier decides, uniformly for the 128 threads, whether to stop
-            // (bit 1) and whether this tile needs the low part of P (bit 0).
-            volatile int* flags = &ctl->tile_flags[jj % 3];
-            const int mine = (ok ? 0 : 2) | ((pmax > kLowPartShare * (l + psum)) ? 1 : 0);
-            if (mine) atomicOr(const_cast<int*>(flags), mine);
-            named_bar_sync(1, kSoftmaxThreads);
-            const int tf = *flags;
-            if (tf & 2) {
-                ok = false;
-                break;
-            }
-            const bool need_lo = tf & 1;
-            if (r == 0) {
-                ctl->tile_flags[(jj + 2) % 3] = 0;  // read by everyone before this barrier; next used by tile jj + 2
-                ctl->lo_flag[x] = need_lo ? 1 : 0;
-            }
-            // ---- P -> shared memory (K-major rows of 64 keys, 128-byte swizzle) ----
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                uint4 w;
-                w.x = pack_bf16x2(s[8 * u + 0], s[8 * u + 1]);
-                w.y = pack_bf16x2(s[8 * u + 2], s[8 * u + 3]);
-                w.z = pack_bf16x2(s[8 * u + 4], s[8 * u + 5]);
-                w.w = pack_bf16x2(s[8 * u + 6], s[8 * u + 7]);
-                const uint32_t off = (u ^ (r & 7)) << 4;
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off), "r"(w.x), "r"(w.y),
-                             "r"(w.z), "r"(w.w)
-                             : "memory");
-                if (need_lo) {
-                    uint4 v;
-                    v.x = pack_bf16x2(s[8 * u + 0] - bf16lo_to_f32(w.x), s[8 * u + 1] - bf16hi_to_f32(w.x));
-                    v.y = pack_bf16x2(s[8 * u + 2] - bf16lo_to_f32(w.y), s[8 * u + 3] - bf16hi_to_f32(w.y));
-                    v.z = pack_bf16x2(s[8 * u + 4] - bf16lo_to_f32(w.z), s[8 * u + 5] - bf16hi_to_f32(w.z));
-                    v.w = pack_bf16x2(s[8 * u + 6] - bf16lo_to_f32(w.w), s[8 * u + 7] - bf16hi_to_f32(w.w));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + kPBytes + off), "r"(v.x),
-                                 "r"(v.y), "r"(v.z), "r"(v.w)
-                                 : "memory");
+            };
+            if constexpr (kSched == kSchedMerge) {
+                if (sg.kind == kOutTwoSplit) {
+                    two_split_merge(sg, own, lse_v);
+                    g += n;
+                    continue;
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            // The normaliser uses the fp32 weights.  Without the low part the bf16
-            // weights that PV sees differ from them by unbiased rounding of at most
-            // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
-            l += psum;
-            mbar_arrive(&ctl->p_full[x]);
+            if constexpr (kPersistent) {
+                if (sg.kind == kOutPiece) {
+                    piece_merge(own, lse_v, g + n);
+                    g += n;
+                    continue;
+                }
+            }
+            {
+                const long long slot_row = static_cast<long long>(sg.split - p.split_base) * out_rows + grow;
+                float* dst = sg.kind == kOutFinal ? p.out + grow * kDLatent + kDLatentHalf * c
+                                                  : p.part_out + slot_row * kDLatent + kDLatentHalf * c;
+                // The rows go out through shared memory so that every store instruction
+                // writes whole 128-byte lines: the thread of a row puts 32 of its values
+                // into the warp's 4 KB tile (swizzled), then each lane stores 16 bytes of
+                // one of four rows.  The P buffers are free here (PV is done).  A warp's
+                // 32 rows belong to one token, so row_valid is warp-uniform.
+                float* wdst = dst - static_cast<long long>(lane) * kDLatent;   // the warp's first row
+                for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                    float v[32];
+                    own(part, v);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), v[4 * u], v[4 * u + 1],
+                                     v[4 * u + 2], v[4 * u + 3]);
+                    __syncwarp();
+                    if (row_valid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int row = 4 * i + (lane >> 3), u = lane & 7;
+                            const float4 v4 = ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
+                            *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) = v4;
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (row_valid && c == 0) {
+                    if (sg.kind == kOutFinal) p.lse[grow] = lse_v;
+                    else p.part_lse[slot_row] = lse_v;
+                }
+            }
+            g += n;
         }
-
-        // ---- epilogue ----
-        if (ok) ok = mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, lim);
-        // one decision for all 128 softmax threads (the two-split merge synchronises them)
-        if constexpr (kMerge) ok = named_bar_and(4, kSoftmaxThreads, ok);
-        else ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (r == 0) {
                 raise_status(p.status, kStatusTimeout);
@@ -1004,57 +1461,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
-        } else if (merge2) {
-            tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
-            two_split_merge([&](int part, float* v) {
-                uint32_t o[32];
-                tmem_ld32(trow + kTmO + 32 * part, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
-            }, lse2 * 0.6931471805599453f);
-        } else {
-            tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            float* dst = (nsplit == 1)
-                             ? p.out + grow * kDLatent + kDLatentHalf * c
-                             : p.part_out + (static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow) *
-                                       kDLatent + kDLatentHalf * c;
-            // The rows go out through shared memory so that every store instruction
-            // writes whole 128-byte lines: the thread of a row puts 32 of its values
-            // into the warp's 4 KB tile (swizzled), then each lane stores 16 bytes of
-            // one of four rows.  The P buffers are free here (PV is done).  A warp's
-            // 32 rows belong to one token, so row_valid is warp-uniform.
-            const uint32_t ebuf = p_addr + q4 * 4096;
-            float* wdst = dst - static_cast<long long>(lane) * kDLatent;   // the warp's first row
-            for (int part = 0; part < kDLatentHalf / 32; ++part) {
-                uint32_t o[32];
-                tmem_ld32(trow + kTmO + 32 * part, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    st_shared_v4(ebuf + lane * 128 + ((u ^ (lane & 7)) << 4), __uint_as_float(o[4 * u]) * inv_l,
-                                 __uint_as_float(o[4 * u + 1]) * inv_l, __uint_as_float(o[4 * u + 2]) * inv_l,
-                                 __uint_as_float(o[4 * u + 3]) * inv_l);
-                __syncwarp();
-                if (row_valid) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = 4 * i + (lane >> 3), u = lane & 7;
-                        const float4 v = ld_shared_v4(ebuf + row * 128 + ((u ^ (row & 7)) << 4));
-                        *reinterpret_cast<float4*>(wdst + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u) = v;
-                    }
-                }
-                __syncwarp();
-            }
-            if (row_valid && c == 0) {
-                const float lse2 = l > 0.f ? m_use + log2f(l) : -INFINITY;
-                const float v = lse2 * 0.6931471805599453f;
-                if (nsplit == 1) p.lse[grow] = v;
-                else p.part_lse[static_cast<long long>(split - p.split_base) * p.total_q * kHeads + grow] = v;
-            }
         }
     }
 

@@ -86,6 +86,12 @@ def test_split_heuristic_and_workspace(lib):
     w4 = binding.workspace_size(16, 512, 32, 16416, splits=4)
     assert w4 - w1 >= 4 * 512 * 64 * 512 * 4
     assert binding.workspace_size(1, 1, 1, 1, num_heads=32) == 0
+    # the persistent schedule: split count 0; its partial slots are sized by the CTA pairs, not the rows
+    assert binding.num_splits(16, 512, 32, 16416, requested=binding.SPLITS_PERSISTENT) == 0
+    assert binding.sparse_num_splits(16, 512, 32, 512, requested=binding.SPLITS_PERSISTENT) == 0
+    assert binding.lib().mla_verify_num_splits(16, 512, 32, 16416, 64, -2) < 0
+    wp = binding.workspace_size(16, 512, 32, 16416, splits=binding.SPLITS_PERSISTENT)
+    assert wp >= 2 * 1 * 128 * 512 * 4 and wp < w4
 
 
 def _kv_call(op, **over):

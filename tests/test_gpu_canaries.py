@@ -71,7 +71,7 @@ def run_guarded(inp, splits=0, topk_idx=None):
     return (out3.cpu().numpy().astype(np.float64), lse2.cpu().numpy().astype(np.float64), status)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 0, -1])
 def test_dense_writes_stay_inside_their_buffers(splits):
     inp = I.make_inputs([700, 64, 2500, 5], [9, 32, 17, 1], tree_kind="forest", seed=31, stream=960)
     out, lse, status = run_guarded(inp, splits)
@@ -90,7 +90,7 @@ def test_tail_cut_writes_stay_inside_their_buffers():
     assert_close(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_o, ref_l, "tail cut, sampled rows")
 
 
-@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("splits", [1, 3, -1])
 def test_sparse_writes_stay_inside_their_buffers(splits):
     inp = I.make_inputs([900, 300, 1500], [6, 9, 3], tree_kind="uniform", seed=32, stream=961)
     topk = I.topk_indices(inp, 100, seed=33)
@@ -98,3 +98,13 @@ def test_sparse_writes_stay_inside_their_buffers(splits):
     assert status == 0
     ref_o, ref_l = oracle.verify_sparse(inp, topk)
     assert_close(out, lse, ref_o, ref_l, f"sparse, {splits} splits")
+
+
+def test_persistent_pieces_write_inside_their_buffers():
+    """Few long items on the persistent schedule: most items are cut between CTA
+    pairs and merged in the kernel; their partial slots live in the workspace."""
+    inp = I.make_inputs([4000, 3000, 5000], [8, 4, 6], tree_kind="uniform", seed=34, stream=962)
+    out, lse, status = run_guarded(inp, -1)
+    assert status == 0
+    ref_o, ref_l = oracle.verify(inp)
+    assert_close(out, lse, ref_o, ref_l, "persistent, cut items")

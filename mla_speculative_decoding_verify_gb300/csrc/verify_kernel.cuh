@@ -342,6 +342,22 @@ __device__ __forceinline__ bool share_segment(const VerifyParams& p, int n_items
     return true;
 }
 
+// Rows of local tile jj of segment s whose partial scores the two CTAs exchange:
+// -1 for all 128, or t for the 64 rows of token t alone.  Sparse tiles of a token's
+// slot list are seen by that token's rows only (the other token's rows are masked
+// out), so half the scores, 16 KB, make the trip.
+template <bool kSparse>
+__device__ __forceinline__ int exchange_rows(const Seg& s, int jj) {
+    if constexpr (kSparse) {
+        int kind, base;
+        sparse_segment(s.t0 + jj, s.nA, s.nB, kind, base);
+        return kind < 2 ? kind : -1;
+    } else {
+        return -1;
+    }
+}
+__host__ __device__ constexpr uint32_t exchange_bytes(int rows) { return rows < 0 ? kXBufBytes : kXBufBytes / 2; }
+
 template <bool kSparse, int kSched>
 __device__ __forceinline__ bool next_segment(const VerifyParams& p, int n_items, Cursor& cu, Seg& s) {
     if constexpr (kSched == kSchedPersistent) {
@@ -621,8 +637,17 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         mbar_init(&ctl->never, 1);
         mbar_init(&ctl->stg_free, 1);
         ctl->abort = 0;
-        // byte count of the first incoming partial, posted before the peer can send
-        mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
+        // byte count of the first incoming partial (the first tile of the first segment
+        // with tiles), posted before the peer can send
+        uint32_t first_bytes = kXBufBytes;
+        if constexpr (kSparse) {
+            Cursor cf = cu0;
+            Seg sf = seg0;
+            bool have = true;
+            while (have && sf.n <= 0) have = next_segment<kSparse, kSched>(p, n_items, cf, sf);
+            if (have) first_bytes = exchange_bytes(exchange_rows<kSparse>(sf, 0));
+        }
+        mbar_arrive_expect_tx(&ctl->x_full, first_bytes);
         fence_mbar_init_cluster();
     }
     if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -966,7 +991,10 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 // the peer has read the partial this CTA sent before (its receive buffer is free)
                 if (t >= 1) ok = mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
                 const bool skip_send = fault_kind() == 3 && sg.item == 0 && sg.split == 0 && c == 0 && t == 1;
-                if (ok && !skip_send) bulk_copy_to_peer(xbuf_peer, stg_local, kXBufBytes, xfull_peer);
+                const int rows = exchange_rows<kSparse>(sg, t - g);   // t lies in the current segment
+                const uint32_t off = rows < 0 ? 0u : static_cast<uint32_t>(rows) * (kXBufBytes / 2);
+                if (ok && !skip_send)
+                    bulk_copy_to_peer(xbuf_peer + off, stg_local + off, exchange_bytes(rows), xfull_peer);
             }
         };
 
@@ -1163,12 +1191,14 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 // Does a later segment of this pair have tiles?  Its first partial then
                 // follows this segment's last one, and its byte count is posted in time.
                 bool more = false;
+                uint32_t more_bytes = kXBufBytes;   // size of that first partial
                 if constexpr (kPersistent) {
                     Cursor c2 = cu;
                     Seg s2;
                     while (next_segment<kSparse, kSched>(p, n_items, c2, s2))
                         if (s2.n > 0) {
                             more = true;
+                            more_bytes = exchange_bytes(exchange_rows<kSparse>(s2, 0));
                             break;
                         }
                 }
@@ -1241,7 +1271,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     named_bar_sync(2, kSoftmaxThreads);
                     if (r == 0 && ok) {
                         if (jj + 1 < n || more) {
-                            mbar_arrive_expect_tx(&ctl->x_full, kXBufBytes);
+                            mbar_arrive_expect_tx(&ctl->x_full, jj + 1 < n ? exchange_bytes(exchange_rows<kSparse>(sg, jj + 1))
+                                                                           : more_bytes);
                             ++posted;
                         }
                         mbar_arrive_remote_relaxed(&ctl->x_empty, peer);

@@ -202,3 +202,18 @@ def test_tail_cut_workspace_only_for_automatic_single_split(lib):
     # the sparse variant (17 tiles at top-k 512) follows the same rule
     assert binding.sparse_workspace_size(16, 512, 32, 512, splits=0) > binding.sparse_workspace_size(16, 512, 32, 512,
                                                                                                     splits=1)
+
+
+def test_automatic_plan_choices(lib):
+    """The plans the split model picks for the five workload shapes and for a
+    uniform 96-item shape (host model only, a 152-SM device assumed when none is
+    present): c1 and c3 one split, c2 two (merged in the kernel), c4 seven,
+    sparse c3 one; the 96-item shape, whose last round of 20 items the per-unit
+    grid cannot cut well, the persistent schedule (0); ragged trees never take it."""
+    assert binding.num_splits(1, 8, 8, 264) == 1
+    assert binding.num_splits(4, 64, 16, 4112) == 2
+    assert binding.num_splits(16, 512, 32, 16416) == 1
+    assert binding.num_splits(2, 128, 64, 65600) == 7
+    assert binding.sparse_num_splits(16, 512, 32, 512) == 1
+    assert binding.num_splits(12, 192, 16, 4112) == 0
+    assert binding.num_splits(12, 191, 16, 4112) != 0          # one request with 15 tree tokens

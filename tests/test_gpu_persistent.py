@@ -140,6 +140,27 @@ def test_persistent_graph_replay_matches_eager_bitwise():
         g.close()
 
 
+def test_persistent_sparse_graph_replay_matches_eager_bitwise():
+    import torch
+    from test_gpu_graph import bucket_inputs, eager, make_graph, replay
+    full = bucket_inputs(kind="forest")
+    idx = I.topk_indices(full, 100, seed=5, unused_frac=0.1, duplicates=True)
+    g = make_graph(full, PERSISTENT, topk=100)
+    try:
+        for k in (6, 3):
+            sub = I.first_requests(full, k)
+            sidx = idx[:sub.total_q]
+            o, l, st = replay(g, sub, sidx)
+            assert st == 0
+            eo, el = eager(sub, PERSISTENT, sidx)
+            assert torch.equal(o, eo) and torch.equal(l, el), f"sparse batch {k}"
+        ref_o, ref_l = oracle.verify_sparse(sub, sidx)
+        assert_close(o.numpy().astype(np.float64), l.numpy().astype(np.float64), ref_o, ref_l,
+                     "persistent sparse replay")
+    finally:
+        g.close()
+
+
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_persistent_full_size_sampled_rows(cfg):
     inp = I.config_inputs(cfg, seed=0)

@@ -72,7 +72,7 @@ def test_split_range_argument_checks():
     ensure_gpu()
     inp = I.make_inputs([300], [4], seed=46, stream=982)
     db = binding.DeviceBatch(inp, "cuda:0")
-    for S, b0, k in ((2, 2, 1), (2, -1, 1), (0, 0, 1), (3, 1, 3)):
+    for S, b0, k in ((2, 2, 1), (2, -1, 1), (0, 0, 1), (3, 1, 3), (binding.SPLITS_PERSISTENT, 0, 1)):
         with pytest.raises(binding.MlaError) as e:
             binding.verify_split_range(db, S, b0, k)
         assert e.value.code == binding.MLA_ERR_INVALID_ARG

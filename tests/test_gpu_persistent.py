@@ -104,6 +104,27 @@ def test_persistent_invalid_requests_zeroed():
     assert_close(out[10:], lse[10:], ref_o[10:], ref_l[10:], "valid request next to invalid ones")
 
 
+def test_persistent_invalid_request_in_a_whole_round():
+    """40 requests x 8 tree tokens (160 items: two whole rounds, then a shared
+    tail); request 3's block table names a page outside the cache, so its items,
+    in the first whole round, carry no tiles and its rows are written as 0 / -inf."""
+    rng = np.random.default_rng(77)
+    prefixes = [int(v) for v in rng.integers(200, 900, size=40)]
+    inp = I.make_inputs(prefixes, [8] * 40, tree_kind="uniform", seed=77, stream=977)
+    rows = I.sample_rows(inp, 600, seed=77)
+    ref_o, ref_l = oracle.verify_rows(inp, rows)
+    inp.block_table = inp.block_table.copy()
+    inp.block_table[3, 2] = inp.num_pages + 1
+    out, lse, status = run_gpu(inp, splits=PERSISTENT)
+    assert status & (1 << binding.MLA_ERR_BAD_BLOCK)
+    bad = slice(int(inp.q_offsets[3]), int(inp.q_offsets[4]))
+    assert not out[bad].any() and np.isneginf(lse[bad]).all()
+    flat_tok = rows // inp.num_heads
+    keep = (flat_tok < bad.start) | (flat_tok >= bad.stop)
+    assert_close(out.reshape(-1, 512)[rows[keep]], lse.reshape(-1)[rows[keep]], ref_o[keep], ref_l[keep],
+                 "valid requests next to an invalid one in a whole round")
+
+
 @pytest.mark.parametrize("topk", [100, 512])
 def test_persistent_sparse(topk):
     inp = I.scaled_config_inputs(3, seed=1, prefix_div=16, batch_cap=4)
@@ -136,6 +157,10 @@ def test_persistent_graph_replay_matches_eager_bitwise():
             assert torch.equal(o, eo) and torch.equal(l, el), f"batch {k}: replay differs from eager"
         ref_o, ref_l = oracle.verify(sub)
         assert_close(o.numpy().astype(np.float64), l.numpy().astype(np.float64), ref_o, ref_l, "persistent replay")
+        # a fully padded replay (no work items, no shares) is a no-op with status 0
+        g.launch(0)
+        torch.cuda.synchronize()
+        assert binding.read_status(g.workspace.data_ptr()) == 0
     finally:
         g.close()
 

@@ -62,10 +62,16 @@ constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
 constexpr int kStages = 3;
 constexpr int kThreads = 224;          // warp 0 TMA, warp 1 QK MMAs, warps 2..5 softmax, warp 6 PV MMAs
-constexpr int kThreadsSparse = 256;    // sparse variant: warps 0 and 7 gather the KV rows
+constexpr int kThreadsSparse = 256;    // sparse variant: warps 0, 6 and 7 gather the KV rows, the softmax issues PV
 constexpr int kGatherWarp2 = 7;
+constexpr int kGatherWarps = 3;        // sparse: warps 0, kPvWarp and kGatherWarp2
+// Sparse gather warp w (0, 1, 2) owns the four-key groups [gather_group0(w),
+// gather_group0(w + 1)) of every 64-key tile: 6, 5 and 5 groups.
+__host__ __device__ constexpr int gather_group0(int w) { return w == 0 ? 0 : w == 1 ? 6 : w == 2 ? 11 : 16; }
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kPvWarp = 6;
+constexpr int kPvWarp = 6;             // dense: the PV issuer; sparse: a gather warp
+static_assert(gather_group0(kGatherWarps) * 4 == 64 && 4 * gather_group0(1) <= 32,
+              "gather warps cover a tile's 64 keys, at most one key per lane");
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kChunkBytes = kBlockN * 64 * 2;          // [64 keys][64 dims] bf16, 128B swizzle
 constexpr uint32_t kRopeTileBytes = kBlockN * kDRopeHalf * 2;  // [64 keys][32 dims], 64B swizzle
@@ -174,7 +180,8 @@ struct Ctrl {
     int lo_flag[2];
     int tile_flags[3];  // per-tile OR of the softmax threads' votes: bit 0 low part of P, bit 1 stop
     int merge_role;     // in-kernel merge: arrival rank of this unit / piece among the row tile's
-    uint32_t slot_mask[kStages][2];  // sparse: bit k of half h set if key 32h + k of the stage's tile is a real slot
+    uint32_t slot_mask[kStages][kGatherWarps];  // sparse: bit k of word w set if key 4 * gather_group0(w) + k of
+                                                // the stage's tile is a real slot
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -566,13 +573,17 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         }
     }
 
-    // Sparse gather warps: lane l of warp h handles key 32h + l of every tile.
-    // The slot values of the first segment's first tiles are loaded before the set-up below.
-    [[maybe_unused]] const int half = warp == 0 ? 0 : 1;
-    [[maybe_unused]] const int key = 32 * half + lane;
+    // Sparse gather warps: lane l of gather warp w handles key 4 * gather_group0(w) + l
+    // of every tile (lanes past the warp's keys none).  The slot values of the first
+    // segment's first tiles are loaded before the set-up below.
+    [[maybe_unused]] const bool gather_warp = kSparse && (warp == 0 || warp == kPvWarp || warp == kGatherWarp2);
+    [[maybe_unused]] const int gw = warp == 0 ? 0 : warp == kPvWarp ? 1 : 2;
+    [[maybe_unused]] const int key0 = 4 * gather_group0(gw);
+    [[maybe_unused]] const int nkeys = 4 * gather_group0(gw + 1) - key0;
+    [[maybe_unused]] const int key = key0 + lane;
     // raw slot value of this lane's key in local tile jj of segment sg (a KV position, -1 for none)
     [[maybe_unused]] auto slot_raw = [&](const Seg& sg, int jj) -> int {
-        if (jj >= sg.n) return -1;
+        if (jj >= sg.n || lane >= nkeys) return -1;
         int kind, base;
         sparse_segment(sg.t0 + jj, sg.nA, sg.nB, kind, base);
         if (kind == 2) return base + key < sg.T ? sg.P + base + key : -1;
@@ -582,7 +593,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     };
     [[maybe_unused]] int pre_raw[3] = {-1, -1, -1};
     if constexpr (kSparse) {
-        if (warp == 0 || warp == kGatherWarp2) {
+        if (gather_warp) {
 #pragma unroll
             for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(seg0, t);
         }
@@ -617,7 +628,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // ---- set-up ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->kv_full[s], kSparse ? 2 : 1);  // sparse: one arrival per gather warp
+            mbar_init(&ctl->kv_full[s], kSparse ? kGatherWarps : 1);  // sparse: one arrival per gather warp
             mbar_init(&ctl->kv_empty[s], 1);
             mbar_init(&ctl->kv_fixed[s], 1);
         }
@@ -669,15 +680,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 
     // The roles below walk the same segments; tile i of the CTA's whole stream
     // (all segments) uses KV stage i % kStages, S buffer and P barriers i & 1.
-    if (warp == 0 || (kSparse && warp == kGatherWarp2)) {
+    if (warp == 0 || gather_warp) {
         // ================= TMA producer(s) =================
-        // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: warps 0
-        // and kGatherWarp2 each own 32 keys of every tile (TMA instructions issued
-        // by the lanes of one warp are serialised, so two warps halve the issue
-        // time).  Lane l looks up the cache row of key 32h + l; lanes 0..7 then
-        // load keys 32h + 4l .. 32h + 4l + 3 with four-row gathers (one box row
-        // per key), and each warp posts its half of the tile's bytes on the stage
-        // barrier, so a gathered tile completes exactly like a dense one.  Empty
+        // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: three
+        // gather warps own 24, 20 and 20 keys of every tile (TMA instructions
+        // issued by the lanes of one warp are serialised, so more warps shorten
+        // the issue time).  Lane l looks up the cache row of the warp's key l;
+        // lane g then loads the warp's keys 4g .. 4g + 3 with four-row gathers
+        // (one box row per key), and each warp posts its share of the tile's bytes
+        // on the stage barrier, so a gathered tile completes exactly like a dense one.  Empty
         // slots name a row past the end of the cache and read as zeros.  The
         // lookups run ahead of the copies: before tile jj waits for its stage,
         // the row of tile jj + 1 is completed and prefetched into L2, and the
@@ -765,12 +776,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                         y[t] = v >= 0 ? v : oob_row;
                     }
                     if (lane == 0) {
-                        ctl->slot_mask[st][half] = mask;
-                        mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes / 2);  // releases the mask with the tile
+                        ctl->slot_mask[st][gw] = mask;
+                        // this warp's share of the stage, 576 bytes per key; releases the mask with the tile
+                        mbar_arrive_expect_tx(&ctl->kv_full[st], static_cast<uint32_t>(nkeys) * (kStageBytes / kBlockN));
                     }
                     __syncwarp();
-                    if (lane < 8) {
-                        const int g = 8 * half + lane;  // keys 4g .. 4g + 3
+                    if (lane < nkeys / 4) {
+                        const int g = key0 / 4 + lane;  // keys 4g .. 4g + 3
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch)
                             tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
@@ -1294,7 +1306,10 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                             const int st = gi % kStages;
                             if (ok) ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
                             const volatile uint32_t* sm = ctl->slot_mask[st];
-                            vis = kind == tok_local ? (static_cast<uint64_t>(sm[1]) << 32) | sm[0] : 0ull;
+                            vis = kind == tok_local ? static_cast<uint64_t>(sm[0]) |
+                                                          (static_cast<uint64_t>(sm[1]) << (4 * gather_group0(1))) |
+                                                          (static_cast<uint64_t>(sm[2]) << (4 * gather_group0(2)))
+                                                    : 0ull;
                         }
 #pragma unroll
                         for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;
@@ -1409,7 +1424,33 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     // weights that PV sees differ from them by unbiased rounding of at most
                     // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
                     l += psum;
-                    mbar_arrive(&ctl->p_full[x]);
+                    if constexpr (kSparse) {
+                        // PV of this tile, issued by one softmax thread once all 128 rows of P
+                        // are in shared memory (the PV warp gathers KV rows in this variant)
+                        named_bar_sync(5, kSoftmaxThreads);
+                        if (r == 0) {
+                            tc_fence_after();
+                            const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+                            const uint64_t ap_hi = smem_desc(p_addr, 16, 1024, kSwizzle128B);
+                            const uint64_t ap_lo = smem_desc(p_addr + kPBytes, 16, 1024, kSwizzle128B);
+                            const int st = gi % kStages;
+                            const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
+                            for (int kk = 0; kk < kBlockN / 16; ++kk)
+                                mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
+                                       (jj > 0 || kk > 0) ? 1u : 0u);
+                            if (need_lo) {
+#pragma unroll
+                                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                                    mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048),
+                                           idesc_pv, 1u);
+                            }
+                            mma_commit(&ctl->pv_done[x]);
+                            mma_commit(&ctl->kv_empty[st]);
+                        }
+                    } else {
+                        mbar_arrive(&ctl->p_full[x]);
+                    }
                 }
                 // ---- epilogue: the segment's last PV ----
                 if (ok) ok = mbar_wait(&ctl->pv_done[(g + n - 1) & 1], ((g + n - 1) >> 1) & 1, abort_flag, lim);
@@ -1492,6 +1533,14 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
+        }
+        if constexpr (kSparse) {
+            // the PV MMAs this thread issued finish before TMEM is released
+            if (r == 0) {
+                const int zero = 0;
+                mma_commit(&ctl->drain_pv);
+                mbar_wait(&ctl->drain_pv, 0, &zero, lim);
+            }
         }
     }
 

@@ -169,6 +169,13 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def plan_key(workload: str, splits: int, topk=None) -> str:
+    """Key of a workload and launch plan in the committed DRAM capture summary."""
+    if topk:
+        return f"{workload}/sparse-top{topk}"
+    return f"{workload}/persistent" if splits == 0 else f"{workload}/{splits}split" + ("s" if splits > 1 else "")
+
+
 def profiled_traffic(workload: str, launch_units: int):
     """DRAM bytes per launch of the fused verify kernel from the committed ncu
     summary, if it was taken on the current kernel sources (else None)."""
@@ -215,9 +222,9 @@ def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7, topk_idx=None)
 # records every configuration: name -> (workload, KV splits (0 = library's
 # choice, -1 = the persistent schedule), top-k slots for the sparse variant or
 # None).  c4 is taken both with 16 splits (its stated configuration) and with
-# the library's choice; c3 also on the persistent schedule.
+# the library's choice.
 SWEEP = {"c2": ("c2", 0, None), "c4_16splits": ("c4", 16, None), "c4": ("c4", 0, None), "c5": ("c5", 0, None),
-         "c3_sparse_top512": ("c3", 0, 512), "c3_persistent": ("c3", -1, None)}
+         "c3_sparse_top512": ("c3", 0, 512)}
 
 
 def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dict:
@@ -276,8 +283,7 @@ def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dic
         k_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
         s_ms = sum(a.elapsed_time(b) for a, b in sev) / steps
         units = int(((inp.n_tree + 1) // 2).sum() * max(splits, 1))
-        traffic_key = (f"{wl}/sparse-top{topk}" if topk else f"{wl}/persistent" if req == -1
-                       else f"{wl}/{splits}splits" if req else wl)
+        traffic_key = plan_key(wl, splits, topk)
         e = {"workload": inp.name, "num_splits": splits, "kernel_ms": k_ms, "step_ms": s_ms,
              "tflops": flops / (k_ms * 1e-3) / 1e12, "kv_gbps": kvb / (k_ms * 1e-3) / 1e9,
              "algorithmic_gflop": flops / 1e9, "device_status": status, "steps": steps,
@@ -512,7 +518,7 @@ def run_ours(args, ranks: Ranks):
     peak = float(peaks["bf16_tflops"])
     # units of one launch = (row tile, split) work units
     units = ((inp.n_tree + 1) // 2).sum() * max(splits, 1)
-    traffic = profiled_traffic(f"{args.workload}/sparse-top{args.topk}" if sparse else args.workload, int(units))
+    traffic = profiled_traffic(plan_key(args.workload, splits, args.topk if sparse else None), int(units))
     if sparse:
         gbs = kv_logical / (t_kern * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",

@@ -246,14 +246,14 @@ long long persistent_rounds(long long items, int pairs) {
 
 // Model of the persistent schedule's time, in the units of model_time: whole-item
 // rounds, then the rest shared evenly over the pairs with one more segment and a
-// merge per pair, every tile 1 % slower than on the per-unit grid (measured on
-// whole rounds of 16 x 16384-token items: 0.7-1.3 %).
+// merge per pair.  A tile costs the same as on the per-unit grid (measured on
+// whole rounds of 24 x 16384-token requests: 2.6855 against 2.6859 ms).
 double persistent_model_time(long long items, int tiles, int pairs) {
     const long long rounds = persistent_rounds(items, pairs);
     const long long rest = items - rounds * pairs;
     double t = static_cast<double>(rounds) * (tiles + kUnitOverheadTiles);
     if (rest > 0) t += static_cast<double>(rest) * tiles / pairs + kUnitOverheadTiles + kMergeTiles;
-    return 1.01 * t;
+    return t;
 }
 
 // Split count for requests of up to `tiles` KV tiles per row tile, or 0 for the
@@ -266,6 +266,8 @@ double persistent_model_time(long long items, int tiles, int pairs) {
 // slower), and when the model puts it at least 5 % ahead.  Measured on 2048- to
 // 32768-token prefixes, it was 2-8 % faster where the per-unit grid's last round
 // was too large to cut in two, and 2-7 % slower elsewhere.
+constexpr double kPersistentMargin = 0.98;
+
 int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
     const long long items_bound = items_bound_of(batch, total_q, max_tree);
     const int pairs = sm_count_of_current() / 2;
@@ -283,8 +285,34 @@ int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
     const int pp = persistent_pairs();
     const bool exact = static_cast<long long>(batch) * max_tree == total_q;
     if (exact && persistent_rounds(items_bound, pp) >= 1 &&
-        persistent_model_time(items_bound, tiles, pp) < 0.95 * best_t)
+        persistent_model_time(items_bound, tiles, pp) < kPersistentMargin * best_t)
         return 0;
+    if (items_bound > 0 && 3 * items_bound <= pairs) {
+        // Latency regime: three or more splits still fit in one wave, so a launch
+        // takes as long as one unit's chain of dependent tiles plus the merge: the
+        // combine kernel for three splits or more, the in-kernel merge for two
+        // (whose variant's longer code costs a small launch more).  Measured step
+        // device times (us) against the choice: 1 x 256 x 8: 29.3 on one split, 31.4
+        // on two, 26.2 on three and five (5 chosen); 1 x 2048 x 8: 89.2 / 64.1 / 34.4
+        // on 1 / 2 / 9; 4 x 512 x 8: 38.6 / 38.5 / 30.4 on 1 / 2 / 3 (3 chosen).
+        const double kTileLatency = 2.1e-6, kMergeFixed = 8.5e-6, kCombineFixed = 4.5e-6;
+        // per row and split: the fp32 partial written and read back, and q loaded again
+        const double kRowSplitBytes = 2048.0 + 2048.0 + 1152.0, kBytesPerSecond = 5.0e12;
+        const long long fit = std::min<long long>(pairs / items_bound, std::min(MLA_MAX_SPLITS, tiles));
+        double t_best = 0.0;
+        int s_best = 1;
+        for (int s = 1; s <= std::max<long long>(1, fit); ++s) {
+            const double t = std::ceil(static_cast<double>(tiles) / s) * kTileLatency +
+                             (s == 1 ? 0.0
+                              : s == 2 ? kMergeFixed
+                                       : kCombineFixed + static_cast<double>(rows) * s * kRowSplitBytes / kBytesPerSecond);
+            if (s == 1 || t < t_best) {
+                t_best = t;
+                s_best = s;
+            }
+        }
+        return s_best;
+    }
     return best;
 }
 

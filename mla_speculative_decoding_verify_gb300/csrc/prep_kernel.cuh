@@ -89,54 +89,97 @@ __device__ void block_exclusive_scan(int n, F f, T* dst, T* warp_sums) {
     __syncthreads();
 }
 
+// Batches up to this size keep their per-request values in shared memory, so
+// that no step reads back from global memory what an earlier step wrote: the
+// kernel's critical path is then two rounds of global loads (the request
+// sizes; the tree parents together with the block tables) instead of about ten.
+constexpr int kStageBatch = 1024;
+static_assert(kLptMaxBatch <= kStageBatch, "longest-first ordering reads the staged lengths");
+
 __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepParams p) {
     grid_launch_dependents();   // the verify kernel may start its launch; it waits for this grid's results
     __shared__ int32_t warp_sums[32];
     __shared__ long long warp_sums64[32];
-    __shared__ int32_t tree_par[kPrepWarps][kMaxTree];
+    __shared__ int8_t tree_par[kPrepWarps][kMaxTree];
     __shared__ uint64_t tree_anc[kPrepWarps][kMaxTree];
+    __shared__ int32_t s_nt[kStageBatch], s_len[kStageBatch], s_state[kStageBatch], s_order[kStageBatch];
+    __shared__ int32_t s_qoff[kStageBatch + 1], s_ioff[kStageBatch + 1];
     const int tid = threadIdx.x;
     const int lane = tid & 31, wid = tid >> 5;
+    const bool staged = p.batch <= kStageBatch;
+    // per-request values: shared memory for staged batches, else global memory
+    // (q_off, req_state, order and item_off are written here: plain loads after a barrier)
+    auto NT = [&](int b) -> int { return staged ? s_nt[b] : __ldg(p.n_tree + b); };
+    auto LEN = [&](int b) -> int { return staged ? s_len[b] : __ldg(p.seq_lens + b); };
+    auto QOFF = [&](int b) -> int { return staged ? s_qoff[b] : p.q_off[b]; };
+    auto STATE = [&](int b) -> int { return staged ? s_state[b] : p.req_state[b]; };
+    auto ORDER = [&](int k) -> int { return staged ? s_order[k] : p.order[k]; };
+    auto IOFF = [&](int k) -> int { return staged ? s_ioff[k] : p.item_off[k]; };
+    if (staged) {
+        for (int b = tid; b < p.batch; b += kPrepThreads) {
+            s_nt[b] = __ldg(p.n_tree + b);
+            s_len[b] = __ldg(p.seq_lens + b);
+        }
+    }
     if (tid == 0) {
         *p.status = 0;
         *p.item_count = 0;
     }
-    __syncthreads();
-
     // 0. sparse variant: no token belongs to a request until step 2 says so
     if (p.tok_req)
         for (int g = tid; g < p.total_q; g += kPrepThreads) p.tok_req[g] = -1;
     if (p.zero_words)
         for (int g = tid; g < p.zero_count; g += kPrepThreads) p.zero_words[g] = 0;
+    __syncthreads();
 
     // 1. query offsets (exclusive scan of n_tree)
-    block_exclusive_scan(p.batch, [&](int b) { return p.n_tree[b]; }, p.q_off, warp_sums);
-    if (tid == 0 && (p.allow_unused_rows ? p.q_off[p.batch] > p.total_q : p.q_off[p.batch] != p.total_q))
+    block_exclusive_scan(p.batch, NT, staged ? s_qoff : p.q_off, warp_sums);
+    if (staged)
+        for (int b = tid; b <= p.batch; b += kPrepThreads) p.q_off[b] = s_qoff[b];
+    if (tid == 0 && (p.allow_unused_rows ? QOFF(p.batch) > p.total_q : QOFF(p.batch) != p.total_q))
         atomicOr(p.status, kStatusBadTree);
 
     // 2. one warp per request: validate sizes, parents and block ids, then the
-    //    ancestor bit sets by pointer jumping (6 rounds cover depth 64)
+    //    ancestor bit sets by pointer jumping (6 rounds cover depth 64).  The
+    //    parents and the block-table entries are loaded together, before either
+    //    is used, so their round trips overlap.
     for (int b = wid; b < p.batch; b += kPrepWarps) {
-        const int T = p.n_tree[b];
-        const int L = p.seq_lens[b];
-        const int base = p.q_off[b];
+        const int T = NT(b);
+        const int L = LEN(b);
+        const int base = QOFF(b);
         const bool shape_ok = T >= 0 && T <= kMaxTree && L >= T && base >= 0 && base + T <= p.total_q;
+        int par[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            par[h] = shape_ok && i < T ? __ldg(p.tree_parent + base + i) : -1;
+        }
         bool bad_parent = false, bad_block = false;
         if (shape_ok) {
-            for (int i = lane; i < T; i += 32) {
-                const int par = p.tree_parent[base + i];
-                const bool good = par >= -1 && par < i;
-                tree_par[wid][i] = good ? par : -1;
-                bad_parent |= !good;
-            }
             const int pages = (L + p.page_size - 1) / p.page_size;
             if (pages > p.max_pages) {
                 bad_block = true;
             } else {
                 const int32_t* row = p.block_table + static_cast<long long>(b) * p.max_pages;
-                for (int k = lane; k < pages; k += 32) {
-                    const int pg = row[k];
-                    bad_block |= pg < 0 || pg >= p.num_pages;
+                for (int k0 = 0; k0 < pages; k0 += 128) {
+                    int pg[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = k0 + 32 * u + lane;
+                        pg[u] = k < pages ? __ldg(row + k) : 0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        bad_block |= k0 + 32 * u + lane < pages && (pg[u] < 0 || pg[u] >= p.num_pages);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i < T) {
+                    const bool good = par[h] >= -1 && par[h] < i;
+                    tree_par[wid][i] = static_cast<int8_t>(good ? par[h] : -1);
+                    bad_parent |= !good;
                 }
             }
         }
@@ -146,7 +189,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
         bad_block = __any_sync(0xffffffffu, bad_block);
         const bool all_ok = shape_ok && !bad_parent && !bad_block;
         if (lane == 0) {
-            p.req_state[b] = shape_ok ? (all_ok ? 0 : 1) : 2;  // 2: outputs not written at all
+            const int state = shape_ok ? (all_ok ? 0 : 1) : 2;  // 2: outputs not written at all
+            p.req_state[b] = state;
+            if (staged) s_state[b] = state;
             const int bits = ((!shape_ok || bad_parent) ? kStatusBadTree : 0) | (bad_block ? kStatusBadBlock : 0);
             if (bits) atomicOr(p.status, bits);
         }
@@ -176,7 +221,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
                     up[h] = nu[h];
                     if (i < T) {
                         tree_anc[wid][i] = a[h];
-                        tree_par[wid][i] = up[h];
+                        tree_par[wid][i] = static_cast<int8_t>(up[h]);
                     }
                 }
                 __syncwarp();
@@ -195,30 +240,31 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
     for (int b = tid; b < p.batch; b += kPrepThreads) {
         int rank = b;
         if (lpt) {
-            const int Lb = p.seq_lens[b];
+            const int Lb = LEN(b);
             rank = 0;
             for (int o = 0; o < p.batch; ++o) {
-                const int Lo = p.seq_lens[o];
+                const int Lo = LEN(o);
                 rank += (Lo > Lb) || (Lo == Lb && o < b);
             }
         }
-        p.order[rank] = b;
+        if (staged) s_order[rank] = b;
+        else p.order[rank] = b;
     }
     __syncthreads();
     block_exclusive_scan(
         p.batch,
         [&](int k) {
-            const int b = p.order[k];
-            return p.req_state[b] == 2 ? 0 : (p.n_tree[b] + kTokensPerTile - 1) / kTokensPerTile;
+            const int b = ORDER(k);
+            return STATE(b) == 2 ? 0 : (NT(b) + kTokensPerTile - 1) / kTokensPerTile;
         },
-        p.item_off, warp_sums);
-    const int total_items = min(p.item_off[p.batch], p.max_items);
+        staged ? s_ioff : p.item_off, warp_sums);
+    const int total_items = min(IOFF(p.batch), p.max_items);
     for (int k = tid; k < p.batch; k += kPrepThreads) {
-        const int b = p.order[k];
-        if (p.req_state[b] == 2) continue;
-        const int cnt = (p.n_tree[b] + kTokensPerTile - 1) / kTokensPerTile;
+        const int b = ORDER(k);
+        if (STATE(b) == 2) continue;
+        const int cnt = (NT(b) + kTokensPerTile - 1) / kTokensPerTile;
         for (int t = 0; t < cnt; ++t) {
-            const int slot = p.item_off[k] + t;
+            const int slot = IOFF(k) + t;
             if (slot < p.max_items) p.items[slot] = make_int2(b, t);
         }
     }
@@ -228,7 +274,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
             const int rem = p.pairs > 0 ? total_items % p.pairs : 0;
             *p.tail_k = (rem > 0 && 2 * rem <= p.pairs) ? min(rem, p.tail_cap) : 0;
         }
-        if (p.item_off[p.batch] > p.max_items) atomicOr(p.status, kStatusBadTree);
+        if (IOFF(p.batch) > p.max_items) atomicOr(p.status, kStatusBadTree);
     }
 
     // 4. persistent schedule: the CTA pairs' shares of all (item, KV tile) positions
@@ -240,14 +286,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
             [&](int k) -> long long {
                 const int2 it = p.items[k];
                 const int b = it.x;
-                if (p.req_state[b] != 0) return 1;   // rows written as out = 0, lse = -inf; no tiles
-                const int T = p.n_tree[b];
+                if (STATE(b) != 0) return 1;   // rows written as out = 0, lse = -inf; no tiles
+                const int T = NT(b);
                 if (p.topk > 0) {
                     const int nA = (p.topk + kBlockN - 1) / kBlockN;
                     const int ntok = min(kTokensPerTile, T - kTokensPerTile * it.y);
                     return static_cast<long long>(nA) * (ntok > 1 ? 2 : 1) + (T + kBlockN - 1) / kBlockN;
                 }
-                return (p.seq_lens[b] + kBlockN - 1) / kBlockN;
+                return (LEN(b) + kBlockN - 1) / kBlockN;
             },
             p.woff, warp_sums64);
         const long long W = p.woff[n];
@@ -297,6 +343,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) mla_prep_kernel(const PrepPar
         }
     }
 }
+
 
 // Sparse variant: every top-k slot must be -1 or a prefix position of its
 // token's request; otherwise the request's rows are written as out = 0,

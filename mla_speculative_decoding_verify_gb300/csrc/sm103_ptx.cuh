@@ -136,6 +136,16 @@ __device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
     return out != 0;
 }
 
+__device__ __forceinline__ void st_shared_u64x2(uint32_t addr, uint64_t a, uint64_t b) {
+    asm volatile("st.shared.v2.u64 [%0], {%1, %2};" ::"r"(addr), "l"(a), "l"(b) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");

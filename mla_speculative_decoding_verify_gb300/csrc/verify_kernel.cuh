@@ -86,7 +86,9 @@ constexpr uint32_t kOffStaging = kOffXBuf + kXBufBytes;         // own partial, 
 constexpr uint32_t kOffP = kOffStaging + kXBufBytes;            // P high part, then P low part
 constexpr uint32_t kOffCtrl = kOffP + 2 * kPBytes;
 constexpr uint32_t kCtrlBytes = 512;
-constexpr uint32_t kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + slack for 1 KB alignment
+constexpr uint32_t kOffVis = kOffCtrl + kCtrlBytes;             // dense: per row, the visibility bits of the
+constexpr uint32_t kVisBytes = kRows * 16;                      // two KV tiles that reach the draft tokens
+constexpr uint32_t kSmemBytes = kOffVis + kVisBytes + 1024;     // + slack for 1 KB alignment
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B swizzle");
 static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0 && kOffP % 1024 == 0,
               "region alignment");
@@ -263,8 +265,7 @@ struct Cursor {
 };
 
 template <bool kSparse>
-__device__ __forceinline__ void seg_item(const VerifyParams& p, int item, Seg& s) {
-    const int2 it = p.items[item];
+__device__ __forceinline__ void seg_item(const VerifyParams& p, int item, int2 it, Seg& s) {
     s.item = item;
     s.b = it.x;
     s.T = __ldg(p.n_tree + s.b);
@@ -293,6 +294,10 @@ __device__ __forceinline__ int item_kv_tiles(const Seg& s) {
 template <bool kSparse, bool kMerge>
 __device__ __forceinline__ bool unit_segment(const VerifyParams& p, int n_items, Seg& s) {
     int item = blockIdx.x >> 1, split = blockIdx.y + p.split_base, nsplit = p.num_splits, share = p.split_share;
+    // the unit's work item, loaded before the item count is known (a cut unit of the
+    // last round loads its own below): the two round trips overlap
+    const int spec = min(item, p.max_items - 1);
+    int2 it = spec >= 0 ? p.items[spec] : make_int2(0, 0);
     int tail_j = -1;
     if (p.tail_k != nullptr) {
         const int k = min(min(__ldg(p.tail_k), p.tail_cap), n_items), whole = n_items - k;
@@ -307,7 +312,8 @@ __device__ __forceinline__ bool unit_segment(const VerifyParams& p, int n_items,
         }
     }
     if (item >= n_items) return false;
-    seg_item<kSparse>(p, item, s);
+    if (item != spec) it = p.items[item];
+    seg_item<kSparse>(p, item, it, s);
     int t0, t1;
     split_range(item_kv_tiles<kSparse>(s), split, nsplit, share, t0, t1);
     s.t0 = t0;
@@ -326,7 +332,8 @@ template <bool kSparse>
 __device__ __forceinline__ bool share_segment(const VerifyParams& p, int n_items, Cursor& cu, Seg& s) {
     if (cu.round < cu.rounds) {
         const int r = cu.round++;
-        seg_item<kSparse>(p, r * p.pairs + ((r & 1) ? p.pairs - 1 - cu.pair : cu.pair), s);
+        const int item = r * p.pairs + ((r & 1) ? p.pairs - 1 - cu.pair : cu.pair);
+        seg_item<kSparse>(p, item, p.items[item], s);
         s.t0 = 0;
         s.n = item_kv_tiles<kSparse>(s);
         s.split = 0;
@@ -336,7 +343,7 @@ __device__ __forceinline__ bool share_segment(const VerifyParams& p, int n_items
     }
     if (cu.x >= cu.end || cu.item >= n_items) return false;
     const long long O = __ldg(p.woff + cu.item), E = __ldg(p.woff + cu.item + 1);
-    seg_item<kSparse>(p, cu.item, s);
+    seg_item<kSparse>(p, cu.item, p.items[cu.item], s);
     const long long a = cu.x - O, e = min(cu.end, E) - O;
     const long long nkv = item_kv_tiles<kSparse>(s);
     s.t0 = static_cast<int>(min(a, nkv));
@@ -392,6 +399,48 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int pair = blockIdx.x >> 1;
+
+    // ---- set-up: barriers, TMEM, the descriptors' prefetch, the cluster sync ----
+    // first_bytes: size of the first incoming partial, posted before the peer can send
+    auto setup = [&](uint32_t first_bytes) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&ctl->kv_full[s], kSparse ? kGatherWarps : 1);  // sparse: one arrival per gather warp
+                mbar_init(&ctl->kv_empty[s], 1);
+                mbar_init(&ctl->kv_fixed[s], 1);
+            }
+            for (int x = 0; x < 2; ++x) {
+                mbar_init(&ctl->s_full[x], 1);
+                mbar_init(&ctl->s_free[x], kSoftmaxThreads);
+                mbar_init(&ctl->p_full[x], kSoftmaxThreads);
+                mbar_init(&ctl->pv_done[x], 1);
+                ctl->lo_flag[x] = 0;
+            }
+            for (int k = 0; k < 3; ++k) ctl->tile_flags[k] = 0;
+            mbar_init(&ctl->x_full, 1);
+            mbar_init(&ctl->x_empty, 1);
+            mbar_init(&ctl->q_ready, kSoftmaxThreads);
+            mbar_init(&ctl->drain_qk, 1);
+            mbar_init(&ctl->drain_pv, 1);
+            mbar_init(&ctl->never, 1);
+            mbar_init(&ctl->stg_free, 1);
+            ctl->abort = 0;
+            mbar_arrive_expect_tx(&ctl->x_full, first_bytes);
+            fence_mbar_init_cluster();
+        }
+        if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
+        if (warp == 0 && lane == 0) {
+            tma_prefetch_desc(&map_lat);
+            tma_prefetch_desc(&map_rope);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        cluster_sync();  // the peer's barriers are initialised before any remote arrive
+    };
+    // The dense kernel sets up while the prep kernel still runs (its first partial
+    // is always a full one); the sparse one needs its first segment for that size.
+    if constexpr (!kSparse) setup(kXBufBytes);
     grid_dependency_wait();     // the prep (and slot check) kernels' work list and metadata
     grid_launch_dependents();
     const int n_items = __ldg(p.item_count);
@@ -407,8 +456,18 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         cu0.rounds = min(__ldg(p.rounds), n_items / max(p.pairs, 1));
         cu0.pair = pair;
     }
+    // An exit before the pipeline starts (both CTAs of the pair take it) gives back
+    // the TMEM of the dense kernel's early set-up; nothing was issued into it.
+    auto release_early = [&]() {
+        if constexpr (!kSparse) {
+            if (warp == 1) tmem_dealloc(ctl->tmem_base, kTmemCols);
+        }
+    };
     Seg seg0;
-    if (!next_segment<kSparse, kSched>(p, n_items, cu0, seg0)) return;
+    if (!next_segment<kSparse, kSched>(p, n_items, cu0, seg0)) {
+        release_early();   // no work for this pair
+        return;
+    }
 
     // rows of this thread (softmax warps only)
     const int q4 = warp & 3;
@@ -555,6 +614,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 #pragma unroll
                         for (int k = 0; k < 32; ++k) v[k] = 0.f;
                     }, -INFINITY);
+                release_early();
                 return;
             }
             if (softmax_warp && tok_local < seg0.ntok) {
@@ -569,6 +629,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     else p.part_lse[slot_row] = -INFINITY;
                 }
             }
+            release_early();
             return;
         }
     }
@@ -625,52 +686,20 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     };
     if (!kSparse && softmax_warp && tok_local < seg0.ntok && seg0.n > 0) issue_q_copies(seg0);
 
-    // ---- set-up ----
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->kv_full[s], kSparse ? kGatherWarps : 1);  // sparse: one arrival per gather warp
-            mbar_init(&ctl->kv_empty[s], 1);
-            mbar_init(&ctl->kv_fixed[s], 1);
-        }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&ctl->s_full[x], 1);
-            mbar_init(&ctl->s_free[x], kSoftmaxThreads);
-            mbar_init(&ctl->p_full[x], kSoftmaxThreads);
-            mbar_init(&ctl->pv_done[x], 1);
-            ctl->lo_flag[x] = 0;
-        }
-        for (int k = 0; k < 3; ++k) ctl->tile_flags[k] = 0;
-        mbar_init(&ctl->x_full, 1);
-        mbar_init(&ctl->x_empty, 1);
-        mbar_init(&ctl->q_ready, kSoftmaxThreads);
-        mbar_init(&ctl->drain_qk, 1);
-        mbar_init(&ctl->drain_pv, 1);
-        mbar_init(&ctl->never, 1);
-        mbar_init(&ctl->stg_free, 1);
-        ctl->abort = 0;
-        // byte count of the first incoming partial (the first tile of the first segment
-        // with tiles), posted before the peer can send
+    // ---- set-up of the sparse kernel ----
+    if constexpr (kSparse) {
+        // byte count of the first incoming partial (the first tile of the first segment with tiles)
         uint32_t first_bytes = kXBufBytes;
-        if constexpr (kSparse) {
+        if (threadIdx.x == 0) {
             Cursor cf = cu0;
             Seg sf = seg0;
             bool have = true;
             while (have && sf.n <= 0) have = next_segment<kSparse, kSched>(p, n_items, cf, sf);
             if (have) first_bytes = exchange_bytes(exchange_rows<kSparse>(sf, 0));
         }
-        mbar_arrive_expect_tx(&ctl->x_full, first_bytes);
-        fence_mbar_init_cluster();
+        setup(first_bytes);
     }
-    if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_lat);
-        tma_prefetch_desc(&map_rope);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    cluster_sync();  // the peer's barriers are initialised before any remote arrive
 
     volatile int* abort_flag = &ctl->abort;
     const uint64_t lim = p.timeout_ns;
@@ -956,6 +985,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
         const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
+        [[maybe_unused]] const uint32_t vis_addr = smem_u32(smem + kOffVis) + r * 16;   // this row's tail-tile masks
         const uint32_t xbuf_peer = mapa(xbuf_local, peer);
         const uint32_t stg_local = smem_u32(smem + kOffStaging);
         const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full), peer);
@@ -1253,6 +1283,18 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 mbar_arrive(&ctl->q_ready);
 
                 const uint64_t anc = row_valid ? p.anc[qidx] : 0ull;
+                // Dense: the KV tiles tmask and tmask + 1 (at most 64 tree tokens) reach the
+                // draft tokens.  Key k of tile tmask is a prefix key (k < a) or tree token
+                // k - a; key k of the next tile is tree token k + 64 - a.  Visible: the prefix
+                // and the row's ancestors and itself.  Taken once per segment, so the tile
+                // loop only selects.
+                [[maybe_unused]] const int tmask = sg.P / kBlockN;
+                if constexpr (!kSparse) {
+                    const int a = sg.P - tmask * kBlockN;
+                    const uint64_t vis_first = (a > 0 ? (1ull << a) - 1ull : 0ull) | (anc << a);
+                    const uint64_t vis_second = a > 0 ? anc >> (kBlockN - a) : 0ull;
+                    st_shared_u64x2(vis_addr, vis_first, vis_second);   // kept out of the registers of the tile loop
+                }
                 stage_and_send(g);
                 for (int jj = 0; jj < n; ++jj) {
                     const int gi = g + jj;
@@ -1295,10 +1337,11 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
                     // the scale is positive, so the row max can be taken on raw scores and the scale
                     // folded into the exponent's FMA below.
+                    uint64_t vis = ~0ull;    // bit k: key k of the tile is visible to this row
+                    bool masked = kSparse;
                     if constexpr (kSparse) {
                         int kind, base;
                         sparse_segment(sg.t0 + jj, sg.nA, sg.nB, kind, base);
-                        uint64_t vis;
                         if (kind == 2) {
                             vis = base == 0 ? anc : 0ull;  // at most 64 tree tokens: one tree tile
                         } else {
@@ -1311,19 +1354,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                                                           (static_cast<uint64_t>(sm[2]) << (4 * gather_group0(2)))
                                                     : 0ull;
                         }
+                    } else {
+                        const int tt = sg.t0 + jj;
+                        masked = tt >= tmask;
+                        if (masked) vis = ld_shared_u64(vis_addr + (tt == tmask ? 0u : 8u));
+                    }
+                    // one compact select per score: this code also runs on a tile's first pass
+                    if (masked) {
 #pragma unroll
                         for (int k = 0; k < kBlockN; ++k) s[k] = ((vis >> k) & 1ull) ? s[k] : -INFINITY;
-                    } else {
-                        const int kpos = (sg.t0 + jj) * kBlockN;
-                        if (kpos + kBlockN > sg.P) {
-#pragma unroll
-                            for (int k = 0; k < kBlockN; ++k) {
-                                const int t = kpos + k;
-                                bool vis = t < sg.P;
-                                if (!vis && t < sg.L) vis = (anc >> (t - sg.P)) & 1ull;
-                                s[k] = vis ? s[k] : -INFINITY;
-                            }
-                        }
                     }
                     // tree reductions (8 independent chains) keep the dependent latency short
                     float mx[8];

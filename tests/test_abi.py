@@ -197,8 +197,9 @@ def test_tail_cut_workspace_only_for_automatic_single_split(lib):
     one = binding.workspace_size(4, 60, 32, 1516, splits=1)
     pairs = 152 // 2                      # no device here: the library assumes 152 SMs
     assert auto - one >= (pairs // 2) * 128 * 512 * 4 * 2
-    # 1 request of 5 KV tiles: too short to cut
-    assert binding.workspace_size(1, 8, 8, 264, splits=0) == binding.workspace_size(1, 8, 8, 264, splits=1)
+    # 40 requests (ragged trees) of 5 KV tiles: one split, too short to cut
+    assert binding.num_splits(40, 319, 8, 264) == 1
+    assert binding.workspace_size(40, 319, 8, 264, splits=0) == binding.workspace_size(40, 319, 8, 264, splits=1)
     # the sparse variant (17 tiles at top-k 512) follows the same rule
     assert binding.sparse_workspace_size(16, 512, 32, 512, splits=0) > binding.sparse_workspace_size(16, 512, 32, 512,
                                                                                                     splits=1)
@@ -207,13 +208,20 @@ def test_tail_cut_workspace_only_for_automatic_single_split(lib):
 def test_automatic_plan_choices(lib):
     """The plans the split model picks for the five workload shapes and for a
     uniform 96-item shape (host model only, a 152-SM device assumed when none is
-    present): c1 and c3 one split, c2 two (merged in the kernel), c4 seven,
-    sparse c3 one; the 96-item shape, whose last round of 20 items the per-unit
-    grid cannot cut well, the persistent schedule (0); ragged trees never take it."""
-    assert binding.num_splits(1, 8, 8, 264) == 1
+    present): c1 five splits (its 4 row tiles fit many times in one wave, so the
+    chain of 5 KV tiles is cut into single tiles and combined), c2 two (merged
+    in the kernel), c3 the persistent schedule (0: its last round of 28 items
+    is shared out), c4 seven, sparse c3 one; the 96-item shape, whose last round
+    of 20 items the per-unit grid cannot cut well, the persistent schedule;
+    ragged trees never take it.  In the one-wave regime the latency model picks
+    three splits or more, never two (the merge variant's fixed cost)."""
+    assert binding.num_splits(1, 8, 8, 264) == 5
     assert binding.num_splits(4, 64, 16, 4112) == 2
-    assert binding.num_splits(16, 512, 32, 16416) == 1
+    assert binding.num_splits(16, 512, 32, 16416) == 0
     assert binding.num_splits(2, 128, 64, 65600) == 7
     assert binding.sparse_num_splits(16, 512, 32, 512) == 1
     assert binding.num_splits(12, 192, 16, 4112) == 0
     assert binding.num_splits(12, 191, 16, 4112) != 0          # one request with 15 tree tokens
+    assert binding.num_splits(4, 32, 8, 520) == 3               # 16 row tiles of 9 KV tiles
+    assert binding.num_splits(1, 8, 8, 16392) == 19             # 4 row tiles of 257 KV tiles: 19 units each
+    assert binding.num_splits(16, 511, 32, 16416) == 1          # ragged: the per-unit grid

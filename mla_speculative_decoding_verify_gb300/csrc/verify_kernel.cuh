@@ -764,6 +764,16 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
             [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
             [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
+            // dense: the block-table entry of the next tile, loaded one tile ahead so that
+            // a freed stage is refilled without a round trip to the table
+            [[maybe_unused]] int pg_next = -1;
+            [[maybe_unused]] auto page_entry = [&](int jt) {
+                return __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages +
+                             (sg.t0 + jt) * kBlockN / p.page_size);
+            };
+            if constexpr (!kSparse) {
+                if (lane == 0) pg_next = page_entry(0);
+            }
             if constexpr (kSparse) {
                 // the first segment's slot values of tiles 0..2 were loaded before the
                 // set-up; the block-table entries of tiles 0 and 1 are one more round trip
@@ -781,6 +791,10 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             for (int jj = 0; jj < n && ok; ++jj) {
                 const int gi = issued;
                 const int st = gi % kStages;
+                [[maybe_unused]] const int pg = pg_next;
+                if constexpr (!kSparse) {
+                    if (lane == 0 && jj + 1 < n) pg_next = page_entry(jj + 1);
+                }
                 if constexpr (kSparse) {
                     if (jj + 1 < n) {
                         nxt = row_of(tpos, page);
@@ -825,8 +839,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 } else {
                     const int kpos = (sg.t0 + jj) * kBlockN;
                     if (lane == 0) {
-                        const int page_idx = kpos / p.page_size;
-                        const int pg = __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages + page_idx);
                         if (pg < 0 || pg >= p.num_pages) raise_status(p.status, kStatusBadBlock);
                         // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
                         const int row = pg * p.page_size + (kpos % p.page_size);

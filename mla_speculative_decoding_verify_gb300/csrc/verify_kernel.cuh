@@ -60,7 +60,7 @@ constexpr int kRows = 128;             // (token, head) rows per CTA
 constexpr int kTokensPerTile = kRows / kHeads;
 constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 224;          // warp 0 TMA, warp 1 QK MMAs, warps 2..5 softmax, warp 6 PV MMAs
 constexpr int kThreadsSparse = 256;    // sparse variant: warps 0, 6 and 7 gather the KV rows, the softmax issues PV
 constexpr int kGatherWarp2 = 7;
@@ -80,27 +80,28 @@ constexpr uint32_t kQRopeBytes = kRows * kDRopeHalf * 2;
 constexpr uint32_t kXBufBytes = kRows * kBlockN * 4;       // one partial score tile, fp32
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kPBytes = kRows * kBlockN * 2;          // one bf16 P tile, K-major, 128B swizzle
 constexpr uint32_t kOffXBuf = kOffQRope + kQRopeBytes;          // receive buffer (the peer's partial)
 constexpr uint32_t kOffStaging = kOffXBuf + kXBufBytes;         // own partial, source of the bulk copy
-constexpr uint32_t kOffP = kOffStaging + kXBufBytes;            // P high part, then P low part
-constexpr uint32_t kOffCtrl = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffCtrl = kOffStaging + kXBufBytes;
 constexpr uint32_t kCtrlBytes = 512;
 constexpr uint32_t kOffVis = kOffCtrl + kCtrlBytes;             // dense: per row, the visibility bits of the
 constexpr uint32_t kVisBytes = kRows * 16;                      // two KV tiles that reach the draft tokens
 constexpr uint32_t kSmemBytes = kOffVis + kVisBytes + 1024;     // + slack for 1 KB alignment
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment for 128B swizzle");
-static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0 && kOffP % 1024 == 0,
-              "region alignment");
+static_assert(kOffQRope % 1024 == 0 && kOffXBuf % 1024 == 0 && kOffStaging % 1024 == 0, "region alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the sm_103 opt-in shared memory per block");
 // the two-split merge copies the other split's 128 rows x 1 KB over the stages, q rope and receive buffer
 static_assert(kOffStaging - kOffStages >= kRows * kDLatentHalf * 4, "merge buffer");
-// the q staging and the persistent merge use the staging and P buffers as one 64 KB region, 16 KB per warp
-static_assert(kOffP == kOffStaging + kXBufBytes && kXBufBytes + 2 * kPBytes >= 4 * 16384, "staging region");
+// Outside the tile loop the staging buffer (32 KB) is scratch, per softmax warp: the q
+// rows of a segment land there in two rounds of 8 KB; an epilogue's rows leave through
+// its first 4 KB tile, the persistent merge reads other pieces' rows through the second.
+static_assert(kXBufBytes == 4 * 8192, "staging region");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384;   // S buffer x at kTmS + 64 * x
-constexpr uint32_t kTmAcc = 256;   // persistent merge: accumulator over the q and S columns (free in an epilogue)
+// TMEM columns: O (fp32, this CTA's 256 dims), q (bf16 pairs), S (fp32, one 64-key tile),
+// P (bf16 pairs: high part, then the low part)
+constexpr uint32_t kTmO = 0, kTmQ = 256, kTmS = 384, kTmP = 448, kTmPLo = 480;
+constexpr uint32_t kTmAcc = 256;   // persistent merge: accumulator over the q, S and P columns (free in an epilogue)
 
 constexpr float kLazyRescaleLog2 = 8.0f;   // rescale only when the max grows by > 2^8
 constexpr float kLowPartShare = 1.0f / 16.0f;
@@ -166,8 +167,8 @@ struct Ctrl {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t kv_fixed[kStages];
-    uint64_t s_full[2];    // QK wrote S buffer x
-    uint64_t s_free[2];    // the softmax threads read S buffer x (QK may overwrite it)
+    uint64_t s_full;       // QK wrote the S columns (one phase per tile)
+    uint64_t s_free;       // the softmax threads read them out (QK may overwrite them)
     uint64_t p_full[2];    // P of tile j is in shared memory (j & 1 selects the barrier)
     uint64_t pv_done[2];   // PV of tile j finished (P buffer and O free again)
     uint64_t x_full;       // the peer's partial of the next tile landed in the receive buffer (bytes)
@@ -410,13 +411,13 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 mbar_init(&ctl->kv_fixed[s], 1);
             }
             for (int x = 0; x < 2; ++x) {
-                mbar_init(&ctl->s_full[x], 1);
-                mbar_init(&ctl->s_free[x], kSoftmaxThreads);
                 mbar_init(&ctl->p_full[x], kSoftmaxThreads);
                 mbar_init(&ctl->pv_done[x], 1);
                 ctl->lo_flag[x] = 0;
             }
             for (int k = 0; k < 3; ++k) ctl->tile_flags[k] = 0;
+            mbar_init(&ctl->s_full, 1);
+            mbar_init(&ctl->s_free, kSoftmaxThreads);
             mbar_init(&ctl->x_full, 1);
             mbar_init(&ctl->x_empty, 1);
             mbar_init(&ctl->q_ready, kSoftmaxThreads);
@@ -500,7 +501,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         int32_t* cnt = p.merge_cnt + (sg.item * 2 + static_cast<int>(c)) * 2;
         float* lse2 = p.part_lse + static_cast<long long>(c) * 2 * part_rows;   // [half][split][row]
         const long long prow = part_row0 + r, pwrow = part_row0 + q4 * 32;   // this row / the warp's first
-        const uint32_t ebuf = smem_u32(smem + kOffP) + q4 * 4096;
+        const uint32_t ebuf = smem_u32(smem + kOffStaging) + q4 * 4096;
         const long long wrow = grow - lane;   // the warp's first row
         named_bar_sync(4, kSoftmaxThreads);
         if (r == 0) ctl->merge_role = atomicAdd(cnt, 1);
@@ -660,31 +661,37 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         }
     }
 
-    // Softmax warps: the query copies of a segment (global -> shared, into the
-    // staging and P buffers, which nothing uses then); the rows move into TMEM
-    // afterwards.  Each warp copies its 32 rows, one whole 512-byte row half per
-    // instruction (unit u of row i at u ^ i), the rope half straight into its
-    // swizzled slot.  The dense kernel starts the first segment's copies before
-    // the set-up; the sparse one after it, so that they do not delay the first
+    // Softmax warps: the query copies of a segment (global -> shared), in two rounds
+    // of 128 features per row through the warp's 8 KB of the staging buffer (which
+    // nothing else uses then); the rows move into TMEM after each round.  Each
+    // instruction copies two 256-byte row pieces (unit u of row i at u ^ (i & 15));
+    // the rope half goes straight into its swizzled slot with the first round.  The
+    // dense kernel starts the first segment's first round before its work item's
+    // KV is known; the sparse one later, so that the copies do not delay the first
     // tile's slot and block-table lookups, which gate its first QK.
-    auto issue_q_copies = [&](const Seg& sg) {
-        const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 16384;
+    auto issue_q_copies = [&](const Seg& sg, int h) {
+        const uint32_t qbuf = smem_u32(smem + kOffStaging) + q4 * 8192;
         const uint32_t qrope = smem_u32(smem + kOffQRope);
         const long long row0 = static_cast<long long>(sg.qbase) * kHeads + q4 * 32;
-        const uint8_t* lat = reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2;
+        const uint8_t* lat =
+            reinterpret_cast<const uint8_t*>(p.q_lat) + (row0 * kDLatent + kDLatentHalf * c) * 2 + 256 * h;
 #pragma unroll 8
-        for (int i = 0; i < 32; ++i)
-            cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4), lat + static_cast<long long>(i) * kDLatent * 2 + 16 * lane);
-        const uint8_t* rope = reinterpret_cast<const uint8_t*>(p.q_rope) + (row0 * kDRope + kDRopeHalf * c) * 2;
+        for (int i = 0; i < 16; ++i) {
+            const int row = 2 * i + (lane >> 4), u = lane & 15;
+            cp_async_16(qbuf + row * 256 + ((u ^ (row & 15)) << 4), lat + static_cast<long long>(row) * kDLatent * 2 + 16 * u);
+        }
+        if (h == 0) {
+            const uint8_t* rope = reinterpret_cast<const uint8_t*>(p.q_rope) + (row0 * kDRope + kDRopeHalf * c) * 2;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = 8 * i + (lane >> 2), u = lane & 3, rr = q4 * 32 + row;
-            cp_async_16(qrope + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4),
-                        rope + static_cast<long long>(row) * kDRope * 2 + 16 * u);
+            for (int i = 0; i < 4; ++i) {
+                const int row = 8 * i + (lane >> 2), u = lane & 3, rr = q4 * 32 + row;
+                cp_async_16(qrope + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4),
+                            rope + static_cast<long long>(row) * kDRope * 2 + 16 * u);
+            }
         }
         cp_async_commit();
     };
-    if (!kSparse && softmax_warp && tok_local < seg0.ntok && seg0.n > 0) issue_q_copies(seg0);
+    if (!kSparse && softmax_warp && tok_local < seg0.ntok && seg0.n > 0) issue_q_copies(seg0, 0);
 
     // ---- set-up of the sparse kernel ----
     if constexpr (kSparse) {
@@ -705,7 +712,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint64_t lim = p.timeout_ns;
     const uint32_t stage0 = smem_u32(smem + kOffStages);
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
-    const uint32_t p_addr = smem_u32(smem + kOffP);
 
     // The roles below walk the same segments; tile i of the CTA's whole stream
     // (all segments) uses KV stage i % kStages, S buffer and P barriers i & 1.
@@ -902,7 +908,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             for (int jj = 0; jj < n; ++jj) {
                 const int gi = g + jj;
                 const int st = gi % kStages;
-                const int x = gi & 1;
                 const bool tail = !kSparse && (sg.t0 + jj) * kBlockN + kBlockN > sg.L;
                 const bool inject = fault_kind() == 1 && sg.item == 0 && sg.split == 0 && c == 0 && jj == 1;
                 if (inject) {
@@ -913,14 +918,14 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 } else {
                     ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
                 }
-                // S buffer x held tile gi - 2; the softmax threads have read it out
-                if (ok && gi >= 2) ok = mbar_wait(&ctl->s_free[x], ((gi - 2) >> 1) & 1, abort_flag, lim);
+                // the S columns held tile gi - 1; the softmax threads have read them out
+                if (ok && gi >= 1) ok = mbar_wait(&ctl->s_free, (gi - 1) & 1, abort_flag, lim);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sb = stage0 + st * kStageBytes;
-                    const uint32_t dS = tmem + kTmS + 64 * x;
+                    const uint32_t dS = tmem + kTmS;
                     // one base descriptor per operand; the k-steps add constant byte offsets
                     const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
                     const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
@@ -931,7 +936,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 #pragma unroll
                     for (int k = 0; k < kDRopeHalf / 16; ++k)
                         mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
-                    mma_commit(&ctl->s_full[x]);
+                    mma_commit(&ctl->s_full);
                 }
                 __syncwarp();
             }
@@ -947,10 +952,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         __syncwarp();
         mbar_wait(&ctl->drain_qk, 0, &zero, lim);
     } else if (warp == kPvWarp) {
-        // ================= PV issuer: O[:, half c] += P * V =================
+        // ================= PV issuer: O[:, half c] += P * V (P in TMEM) =================
         const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
-        const uint64_t ap_hi = smem_desc(p_addr, 16, 1024, kSwizzle128B);
-        const uint64_t ap_lo = smem_desc(p_addr + kPBytes, 16, 1024, kSwizzle128B);
         bool ok = true;
         int g = 0;
         Cursor cu = cu0;
@@ -970,12 +973,12 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
+                        mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     if (lo) {
 #pragma unroll
                         for (int kk = 0; kk < kBlockN / 16; ++kk)
-                            mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                            mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
                     }
                     mma_commit(&ctl->pv_done[x]);
                     mma_commit(&ctl->kv_empty[st]);
@@ -1003,9 +1006,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full), peer);
         const uint32_t rowbase = stg_local + r * (kBlockN * 4);       // this row in the staging buffer
         const uint32_t peerbase = xbuf_local + r * (kBlockN * 4);     // this row in the receive buffer
-        const uint32_t prow = p_addr + r * 128;                       // this row of P (128 bytes)
-        const uint32_t qbuf = stg_local + q4 * 16384;                 // this warp's 16 KB of the staging + P region
-        const uint32_t ebuf = p_addr + q4 * 4096;                     // this warp's 4 KB output tile
+        const uint32_t qbuf = stg_local + q4 * 8192;                  // this warp's 8 KB of the staging buffer (q)
+        const uint32_t ebuf = stg_local + q4 * 4096;                  // this warp's 4 KB output tile
+        const uint32_t mbuf = stg_local + 16384 + q4 * 4096;          // persistent merge: other pieces' rows
         int posted = 1;    // incoming partials whose byte count is posted (thread r == 0)
         int consumed = 0;  // incoming partials waited for (thread r == 0)
         bool ok = true;
@@ -1017,8 +1020,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         // the peer's receive buffer.  Every softmax thread takes part in the named
         // barrier, whatever its `ok`.
         auto stage_and_send = [&](int t) {
-            const int x = t & 1;
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(&ctl->s_full[x], (t >> 1) & 1, abort_flag, lim));
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&ctl->s_full, t & 1, abort_flag, lim));
             // the peer has received the previous partial: the staging buffer may be overwritten
             if (ok && t >= 1) ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->stg_free, (t - 1) & 1, abort_flag, lim));
             if (ok) {
@@ -1026,7 +1028,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t a[32];
-                    tmem_ld32(trow + kTmS + 64 * x + 32 * hh, a);
+                    tmem_ld32(trow + kTmS + 32 * hh, a);
                     tmem_wait_ld();
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -1037,7 +1039,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&ctl->s_free[x]);  // S buffer x may take the next QK
+                mbar_arrive(&ctl->s_free);  // the S columns may take the next QK
                 fence_proxy_async_smem();
             }
             named_bar_sync(3, kSoftmaxThreads);
@@ -1170,17 +1172,18 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     } else {
                         const float* src = p.part_out + (static_cast<long long>(slot_of(q)) * kRows + q4 * 32) * kDLatent +
                                            kDLatentHalf * c;
-                        for (int hh = 0; hh < 2; ++hh) {
-                            // 32 rows x 128 columns: unit u of row i at u ^ i
-#pragma unroll 8
-                            for (int i = 0; i < 32; ++i)
-                                cp_async_16(qbuf + i * 512 + ((lane ^ i) << 4),
-                                            src + static_cast<long long>(i) * kDLatent + 128 * hh + 4 * lane);
+                        for (int part = 0; part < kDLatentHalf / 32; ++part) {
+                            // 32 rows x 32 columns: unit u of row i at u ^ (i & 7)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int row = 4 * i + (lane >> 3), u = lane & 7;
+                                cp_async_16(mbuf + row * 128 + ((u ^ (row & 7)) << 4),
+                                            src + static_cast<long long>(row) * kDLatent + 32 * part + 4 * u);
+                            }
                             cp_async_commit();
                             cp_async_wait<0>();
                             __syncwarp();
-                            for (int pp = 0; pp < 4; ++pp) {
-                                const int part = 4 * hh + pp;
+                            {
                                 uint32_t a[32];
                                 if (k > 0) {
                                     tmem_ld32(trow + kTmAcc + 32 * part, a);
@@ -1188,7 +1191,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                                 }
 #pragma unroll
                                 for (int u = 0; u < 8; ++u) {
-                                    const float4 t = ld_shared_v4(qbuf + lane * 512 + (((8 * pp + u) ^ lane) << 4));
+                                    const float4 t = ld_shared_v4(mbuf + lane * 128 + ((u ^ (lane & 7)) << 4));
                                     const float o4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -1206,8 +1209,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 }
                 ++k;
             }
-            // the merged rows leave through the warp's 4 KB tile in whole 128-byte lines; the
-            // tiles of warps 0..3 lie in the 16 KB slice of warp 2, which may still be reading
+            // the merged rows leave through the warp's 4 KB tile in whole 128-byte lines
             named_bar_sync(4, kSoftmaxThreads);
             if (row_valid) {
                 float* wdst = p.out + (grow - lane) * kDLatent + kDLatentHalf * c;
@@ -1257,9 +1259,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                         }
                 }
                 // ---- q of the segment -> TMEM columns [kTmQ, kTmQ + 128), rope half -> shared memory ----
-                // The warp's async copies land in its 16 KB slice of the staging and P
-                // buffers; then the thread of each row moves the row into TMEM.  A
-                // warp's rows belong to one token, so row_valid is warp-uniform; rows
+                // The warp's async copies land in its 8 KB of the staging buffer, half a
+                // row at a time; then the thread of each row moves that half into TMEM.
+                // A warp's rows belong to one token, so row_valid is warp-uniform; rows
                 // of a missing second token are zeros.  A later segment reuses the
                 // staging buffer once this CTA's last partial-score copy has landed;
                 // the previous segment's QK and PV are complete by then.
@@ -1268,26 +1270,30 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     ok = named_bar_and(4, kSoftmaxThreads, sok);
                     if (!ok) break;
                 }
-                if (row_valid) {
-                    if (kSparse || !first) issue_q_copies(sg);
-                    cp_async_wait<0>();
-                } else {
-                    for (int u = 0; u < 4; ++u)
-                        st_shared_v4(qrope_addr + r * 64 + ((u ^ ((r >> 1) & 3)) << 4), 0.f, 0.f, 0.f, 0.f);
-                }
-                __syncwarp();
-                for (int part = 0; part < 4; ++part) {
-                    uint32_t v[32];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const float4 w = row_valid ? ld_shared_v4(qbuf + lane * 512 + (((8 * part + u) ^ lane) << 4))
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[4 * u + 0] = __float_as_uint(w.x);
-                        v[4 * u + 1] = __float_as_uint(w.y);
-                        v[4 * u + 2] = __float_as_uint(w.z);
-                        v[4 * u + 3] = __float_as_uint(w.w);
+                for (int h = 0; h < 2; ++h) {
+                    if (row_valid) {
+                        if (h == 1 || kSparse || !first) issue_q_copies(sg, h);
+                        cp_async_wait<0>();
+                    } else if (h == 0) {
+                        for (int u = 0; u < 4; ++u)
+                            st_shared_v4(qrope_addr + r * 64 + ((u ^ ((r >> 1) & 3)) << 4), 0.f, 0.f, 0.f, 0.f);
                     }
-                    tmem_st32(trow + kTmQ + 32 * part, v);
+                    __syncwarp();
+                    for (int pp = 0; pp < 2; ++pp) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const float4 w = row_valid
+                                                 ? ld_shared_v4(qbuf + lane * 256 + (((8 * pp + u) ^ (lane & 15)) << 4))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v[4 * u + 0] = __float_as_uint(w.x);
+                            v[4 * u + 1] = __float_as_uint(w.y);
+                            v[4 * u + 2] = __float_as_uint(w.z);
+                            v[4 * u + 3] = __float_as_uint(w.w);
+                        }
+                        tmem_st32(trow + kTmQ + 32 * (2 * h + pp), v);
+                    }
+                    __syncwarp();   // this half is read out before the next one lands
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
@@ -1446,30 +1452,24 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                         ctl->tile_flags[(gi + 2) % 3] = 0;  // read by everyone before this barrier; next used by tile gi + 2
                         ctl->lo_flag[x] = need_lo ? 1 : 0;
                     }
-                    // ---- P -> shared memory (K-major rows of 64 keys, 128-byte swizzle) ----
+                    // ---- P -> TMEM: keys 2k and 2k + 1 of the tile as the bf16 pair in column k of
+                    // this row (the A operand of PV), the low part in the next 32 columns ----
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(s[8 * u + 0], s[8 * u + 1]);
-                        w.y = pack_bf16x2(s[8 * u + 2], s[8 * u + 3]);
-                        w.z = pack_bf16x2(s[8 * u + 4], s[8 * u + 5]);
-                        w.w = pack_bf16x2(s[8 * u + 6], s[8 * u + 7]);
-                        const uint32_t off = (u ^ (r & 7)) << 4;
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + off), "r"(w.x), "r"(w.y),
-                                     "r"(w.z), "r"(w.w)
-                                     : "memory");
+                    for (int hh = 0; hh < 2; ++hh) {   // 16 columns (32 keys) at a time
+                        uint32_t ph[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) ph[k] = pack_bf16x2(s[32 * hh + 2 * k], s[32 * hh + 2 * k + 1]);
+                        tmem_st16(trow + kTmP + 16 * hh, ph);
                         if (need_lo) {
-                            uint4 v;
-                            v.x = pack_bf16x2(s[8 * u + 0] - bf16lo_to_f32(w.x), s[8 * u + 1] - bf16hi_to_f32(w.x));
-                            v.y = pack_bf16x2(s[8 * u + 2] - bf16lo_to_f32(w.y), s[8 * u + 3] - bf16hi_to_f32(w.y));
-                            v.z = pack_bf16x2(s[8 * u + 4] - bf16lo_to_f32(w.z), s[8 * u + 5] - bf16hi_to_f32(w.z));
-                            v.w = pack_bf16x2(s[8 * u + 6] - bf16lo_to_f32(w.w), s[8 * u + 7] - bf16hi_to_f32(w.w));
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + kPBytes + off),
-                                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                         : "memory");
+                            uint32_t pl[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                pl[k] = pack_bf16x2(s[32 * hh + 2 * k] - bf16lo_to_f32(ph[k]),
+                                                    s[32 * hh + 2 * k + 1] - bf16hi_to_f32(ph[k]));
+                            tmem_st16(trow + kTmPLo + 16 * hh, pl);
                         }
                     }
-                    fence_proxy_async_smem();
+                    tmem_wait_st();
                     tc_fence_before();
                     // The normaliser uses the fp32 weights.  Without the low part the bf16
                     // weights that PV sees differ from them by unbiased rounding of at most
@@ -1477,24 +1477,21 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     l += psum;
                     if constexpr (kSparse) {
                         // PV of this tile, issued by one softmax thread once all 128 rows of P
-                        // are in shared memory (the PV warp gathers KV rows in this variant)
+                        // are in TMEM (the PV warp gathers KV rows in this variant)
                         named_bar_sync(5, kSoftmaxThreads);
                         if (r == 0) {
                             tc_fence_after();
                             const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
-                            const uint64_t ap_hi = smem_desc(p_addr, 16, 1024, kSwizzle128B);
-                            const uint64_t ap_lo = smem_desc(p_addr + kPBytes, 16, 1024, kSwizzle128B);
                             const int st = gi % kStages;
                             const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
                             for (int kk = 0; kk < kBlockN / 16; ++kk)
-                                mma_ss(tmem + kTmO, desc_advance(ap_hi, kk * 32), desc_advance(bv, kk * 2048), idesc_pv,
+                                mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
                                        (jj > 0 || kk > 0) ? 1u : 0u);
                             if (need_lo) {
 #pragma unroll
                                 for (int kk = 0; kk < kBlockN / 16; ++kk)
-                                    mma_ss(tmem + kTmO, desc_advance(ap_lo, kk * 32), desc_advance(bv, kk * 2048),
-                                           idesc_pv, 1u);
+                                    mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
                             }
                             mma_commit(&ctl->pv_done[x]);
                             mma_commit(&ctl->kv_empty[st]);
@@ -1505,6 +1502,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 }
                 // ---- epilogue: the segment's last PV ----
                 if (ok) ok = mbar_wait(&ctl->pv_done[(g + n - 1) & 1], ((g + n - 1) >> 1) & 1, abort_flag, lim);
+                // the staging buffer, the epilogue's scratch, was the source of the CTA's last
+                // partial-score copy: wait until it has landed
+                if (ok) ok = mbar_wait<true>(&ctl->stg_free, (g + n - 1) & 1, abort_flag, lim);
             }
             // one decision for all 128 softmax threads (the in-kernel merges and the next
             // segment synchronise them)

@@ -222,9 +222,9 @@ def cpu_baseline(inp, flops_total: int, rows: int, seed: int = 7, topk_idx=None)
 # records every configuration: name -> (workload, KV splits (0 = library's
 # choice, -1 = the persistent schedule), top-k slots for the sparse variant or
 # None).  c4 is taken both with 16 splits (its stated configuration) and with
-# the library's choice.
+# the library's choice; c3 also on the persistent schedule.
 SWEEP = {"c2": ("c2", 0, None), "c4_16splits": ("c4", 16, None), "c4": ("c4", 0, None), "c5": ("c5", 0, None),
-         "c3_sparse_top512": ("c3", 0, 512)}
+         "c3_sparse_top512": ("c3", 0, 512), "c3_persistent": ("c3", -1, None)}
 
 
 def sweep_workloads(args, ranks: Ranks, steps: int = 10, warmup: int = 3) -> dict:

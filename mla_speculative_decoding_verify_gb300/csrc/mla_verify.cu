@@ -246,14 +246,20 @@ long long persistent_rounds(long long items, int pairs) {
 
 // Model of the persistent schedule's time, in the units of model_time: whole-item
 // rounds, then the rest shared evenly over the pairs with one more segment and a
-// merge per pair.  A tile costs the same as on the per-unit grid (measured on
-// whole rounds of 24 x 16384-token requests: 2.6855 against 2.6859 ms).
+// merge per pair, every tile kPersistentTileCost times as long as on the per-unit
+// grid.  Whole rounds of 24 x 16384-token requests measured 2.3 % slower (2.518
+// against 2.462 ms: the persistent variant has no registers to spare for the
+// four-stage pipeline and spills a little); 8 % is fitted to a sweep of eleven
+// uniform shapes, on which the model then picks the faster schedule every time
+// (persistent only for 12 x 8192 x 16: 0.3666 against 0.3707 ms).
+constexpr double kPersistentTileCost = 1.08;
+
 double persistent_model_time(long long items, int tiles, int pairs) {
     const long long rounds = persistent_rounds(items, pairs);
     const long long rest = items - rounds * pairs;
     double t = static_cast<double>(rounds) * (tiles + kUnitOverheadTiles);
     if (rest > 0) t += static_cast<double>(rest) * tiles / pairs + kUnitOverheadTiles + kMergeTiles;
-    return t;
+    return kPersistentTileCost * t;
 }
 
 // Split count for requests of up to `tiles` KV tiles per row tile, or 0 for the
@@ -263,10 +269,8 @@ double persistent_model_time(long long items, int tiles, int pairs) {
 // then the item count is exact, and the rounds the model counts are the real
 // ones), with at least one round of whole items (with none, pairs stream one
 // request's KV at different offsets and lose its reuse in L2; measured 1-3 %
-// slower), and when the model puts it at least 5 % ahead.  Measured on 2048- to
-// 32768-token prefixes, it was 2-8 % faster where the per-unit grid's last round
-// was too large to cut in two, and 2-7 % slower elsewhere.
-constexpr double kPersistentMargin = 0.98;
+// slower), and when the model puts it at least 5 % ahead.
+constexpr double kPersistentMargin = 0.95;
 
 int choose_splits_tiles(int batch, int total_q, int max_tree, int tiles) {
     const long long items_bound = items_bound_of(batch, total_q, max_tree);

@@ -210,18 +210,18 @@ def test_automatic_plan_choices(lib):
     uniform 96-item shape (host model only, a 152-SM device assumed when none is
     present): c1 five splits (its 4 row tiles fit many times in one wave, so the
     chain of 5 KV tiles is cut into single tiles and combined), c2 two (merged
-    in the kernel), c3 the persistent schedule (0: its last round of 28 items
-    is shared out), c4 seven, sparse c3 one; the 96-item shape, whose last round
-    of 20 items the per-unit grid cannot cut well, the persistent schedule;
-    ragged trees never take it.  In the one-wave regime the latency model picks
-    three splits or more, never two (the merge variant's fixed cost)."""
+    in the kernel), c3 one (the last round's 28 items cut in two), c4 seven,
+    sparse c3 one; 12 x 8192 x 16 (96 items, whose last round of 20 the per-unit
+    grid cannot cut well) the persistent schedule (0); ragged trees never take
+    it.  In the one-wave regime the latency model picks three splits or more,
+    never two (the merge variant's fixed cost)."""
     assert binding.num_splits(1, 8, 8, 264) == 5
     assert binding.num_splits(4, 64, 16, 4112) == 2
-    assert binding.num_splits(16, 512, 32, 16416) == 0
+    assert binding.num_splits(16, 512, 32, 16416) == 1
     assert binding.num_splits(2, 128, 64, 65600) == 7
     assert binding.sparse_num_splits(16, 512, 32, 512) == 1
-    assert binding.num_splits(12, 192, 16, 4112) == 0
-    assert binding.num_splits(12, 191, 16, 4112) != 0          # one request with 15 tree tokens
+    assert binding.num_splits(12, 192, 16, 8208) == 0
+    assert binding.num_splits(12, 191, 16, 8208) != 0          # one request with 15 tree tokens
     assert binding.num_splits(4, 32, 8, 520) == 3               # 16 row tiles of 9 KV tiles
     assert binding.num_splits(1, 8, 8, 16392) == 19             # 4 row tiles of 257 KV tiles: 19 units each
     assert binding.num_splits(16, 511, 32, 16416) == 1          # ragged: the per-unit grid

@@ -200,10 +200,10 @@ def test_persistent_full_size_sampled_rows(cfg):
 
 
 def test_automatic_choice_takes_persistent_on_a_short_last_round():
-    """12 requests x 16 tree tokens x 4096: 96 work items on 76 CTA pairs.  The
+    """12 requests x 16 tree tokens x 8192: 96 work items on 76 CTA pairs.  The
     per-unit grid would leave a last round of 20 items; the automatic choice
     takes the persistent schedule (split count 0), and it matches the oracle."""
-    inp = I.make_inputs([4096] * 12, [16] * 12, tree_kind="uniform", seed=6, stream=976)
+    inp = I.make_inputs([8192] * 12, [16] * 12, tree_kind="uniform", seed=6, stream=976)
     ensure_gpu()
     assert binding.num_splits(inp.batch, inp.total_q, inp.max_tree, inp.max_seq_len) == 0
     out, lse, status = run_gpu(inp, splits=0)

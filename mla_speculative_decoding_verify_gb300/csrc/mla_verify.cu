@@ -448,9 +448,18 @@ int mla_init(int device) {
                            reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedPlain>),
                            reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedMerge>),
                            reinterpret_cast<const void*>(mla::mla_verify_kernel<true, mla::kSchedPersistent>)})
+    {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(mla::kSmemBytes)) !=
             cudaSuccess)
             return MLA_ERR_CUDA;
+        // The warpgroups' register shares must fit in what the block is launched with,
+        // or the softmax warps' setmaxnreg.inc would never complete: refuse to run.
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return MLA_ERR_CUDA;
+        if (static_cast<long long>(fa.numRegs) * mla::kThreads <
+            128LL * mla::kRegsSoftmax + 256LL * mla::kRegsOther)
+            return MLA_ERR_UNSUPPORTED;
+    }
     g_dev[device].sm_count = prop.multiProcessorCount;
     // 2-CTA clusters of the verify kernel resident at once (one CTA per SM; the
     // placement of clusters may leave SMs out), the grid of the persistent schedule

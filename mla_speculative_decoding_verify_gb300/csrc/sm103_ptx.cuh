@@ -182,6 +182,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
+// Warpgroup register reallocation: every warp of the warpgroup executes the same one.
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

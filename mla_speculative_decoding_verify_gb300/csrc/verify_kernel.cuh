@@ -61,15 +61,32 @@ constexpr int kTokensPerTile = kRows / kHeads;
 constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
 constexpr int kStages = 4;
-constexpr int kThreads = 224;          // warp 0 TMA, warp 1 QK MMAs, warps 2..5 softmax, warp 6 PV MMAs
-constexpr int kThreadsSparse = 256;    // sparse variant: warps 0, 6 and 7 gather the KV rows, the softmax issues PV
-constexpr int kGatherWarp2 = 7;
+// Three warpgroups.  Warpgroup 0: warp 0 TMA producer, warp 1 QK MMAs, warp 2 PV MMAs
+// (dense; sparse: warps 0, 2 and 3 gather the KV rows and the softmax issues PV).
+// Warpgroup 1 (warps 4..7): softmax, one thread per row.  Warpgroup 2 (warps 8..11):
+// the exchange, partial scores from TMEM through the staging buffer to the peer.
+// Warp w reaches TMEM lanes [32 (w % 4), 32 (w % 4) + 32), so each row-owning
+// warpgroup covers the 128 lanes.
+constexpr int kThreads = 384;
+constexpr int kThreadsSparse = 384;
+constexpr int kGatherWarp2 = 3;
 constexpr int kGatherWarps = 3;        // sparse: warps 0, kPvWarp and kGatherWarp2
 // Sparse gather warp w (0, 1, 2) owns the four-key groups [gather_group0(w),
 // gather_group0(w + 1)) of every 64-key tile: 6, 5 and 5 groups.
 __host__ __device__ constexpr int gather_group0(int w) { return w == 0 ? 0 : w == 1 ? 6 : w == 2 ? 11 : 16; }
-constexpr int kSoftmaxWarp0 = 2;
-constexpr int kPvWarp = 6;             // dense: the PV issuer; sparse: a gather warp
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kStagerWarp0 = 8;
+constexpr int kPvWarp = 2;             // dense: the PV issuer; sparse: a gather warp
+// Register split (setmaxnreg).  An increase draws only on the registers the block was
+// launched with, so the three warpgroups' shares must add up to at most the launch's
+// total: 384 threads at 168 each (the most __launch_bounds__(384, 1) allows) hold
+// 64,512 = 128 x 232 (softmax) + 256 x 136 (the others).  The host checks the compiled
+// register count against this before the first launch (a larger split would wait
+// forever).
+constexpr int kRegsAtLaunch = 168, kRegsSoftmax = 232, kRegsOther = 136;
+static_assert(128 * kRegsSoftmax + 256 * kRegsOther <= 384 * kRegsAtLaunch, "register split above the launch total");
+static_assert(kRegsSoftmax % 8 == 0 && kRegsOther % 8 == 0, "setmaxnreg counts are multiples of 8");
+static_assert(kThreads == 3 * 128 && kThreadsSparse == 3 * 128, "three warpgroups");
 static_assert(gather_group0(kGatherWarps) * 4 == 64 && 4 * gather_group0(1) <= 32,
               "gather warps cover a tile's 64 keys, at most one key per lane");
 constexpr int kSoftmaxThreads = 128;
@@ -174,6 +191,8 @@ struct Ctrl {
     uint64_t x_full;       // the peer's partial of the next tile landed in the receive buffer (bytes)
     uint64_t x_empty;      // the peer finished reading the partial this CTA sent it
     uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
+    uint64_t staged;       // the exchange warps put the own partial of the next tile in the staging buffer
+    uint64_t stg_read;     // the softmax threads have read it (the exchange warps may overwrite it)
     uint64_t q_ready;      // q of the next segment is in TMEM / shared memory (one phase per segment)
     uint64_t drain_qk;
     uint64_t drain_pv;
@@ -197,7 +216,7 @@ __device__ __forceinline__ void raise_status(int* status, int bit) { atomicOr(st
 //   1  the QK issuer waits for KV tile 1 on a barrier that nothing completes;
 //   2  (two splits merged in the kernel) the first unit of the row tile never
 //      marks its partial written, so the second one's poll runs out;
-//   3  the softmax threads do not send the partial scores of tile 1;
+//   3  the exchange warps do not send the partial scores of tile 1;
 //   4  (persistent schedule) the pieces of cut items other than the last never
 //      mark their partials written, so the last one's poll runs out.
 #ifdef MLA_FAULT_INJECTION
@@ -425,6 +444,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             mbar_init(&ctl->drain_pv, 1);
             mbar_init(&ctl->never, 1);
             mbar_init(&ctl->stg_free, 1);
+            mbar_init(&ctl->staged, 1);
+            mbar_init(&ctl->stg_read, 1);
             ctl->abort = 0;
             mbar_arrive_expect_tx(&ctl->x_full, first_bytes);
             fence_mbar_init_cluster();
@@ -476,6 +497,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const int tok_local = r / kHeads;
     const int head = r % kHeads;
     const bool softmax_warp = warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4;
+    const bool stager_warp = warp >= kStagerWarp0 && warp < kStagerWarp0 + 4;
     const long long out_rows = static_cast<long long>(p.total_q) * kHeads;
 
     // ---- two-split merge (per-unit grid; softmax warps) ----
@@ -639,6 +661,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // of every tile (lanes past the warp's keys none).  The slot values of the first
     // segment's first tiles are loaded before the set-up below.
     [[maybe_unused]] const bool gather_warp = kSparse && (warp == 0 || warp == kPvWarp || warp == kGatherWarp2);
+    static_assert(kGatherWarp2 < kSoftmaxWarp0 && kPvWarp < kSoftmaxWarp0, "producer roles in warpgroup 0");
     [[maybe_unused]] const int gw = warp == 0 ? 0 : warp == kPvWarp ? 1 : 2;
     [[maybe_unused]] const int key0 = 4 * gather_group0(gw);
     [[maybe_unused]] const int nkeys = 4 * gather_group0(gw + 1) - key0;
@@ -714,7 +737,11 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     const uint32_t qrope_addr = smem_u32(smem + kOffQRope);
 
     // The roles below walk the same segments; tile i of the CTA's whole stream
-    // (all segments) uses KV stage i % kStages, S buffer and P barriers i & 1.
+    // (all segments) uses KV stage i % kStages and P barriers i & 1.  Each
+    // warpgroup's branch starts with its register reallocation: warpgroup 1 (softmax)
+    // takes the registers that warpgroups 0 and 2 give back.
+    if (warp < kSoftmaxWarp0) {
+    setmaxnreg_dec<kRegsOther>();
     if (warp == 0 || gather_warp) {
         // ================= TMA producer(s) =================
         // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: three
@@ -995,15 +1022,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         if (lane == 0) mma_commit(&ctl->drain_pv);
         __syncwarp();
         mbar_wait(&ctl->drain_pv, 0, &zero, lim);
+    }
     } else if (softmax_warp) {
+        setmaxnreg_inc<kRegsSoftmax>();
         // ================= softmax / epilogue (thread = row) =================
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t trow = tmem + lane_base;
         const uint32_t xbuf_local = smem_u32(smem + kOffXBuf);
         [[maybe_unused]] const uint32_t vis_addr = smem_u32(smem + kOffVis) + r * 16;   // this row's tail-tile masks
-        const uint32_t xbuf_peer = mapa(xbuf_local, peer);
         const uint32_t stg_local = smem_u32(smem + kOffStaging);
-        const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full), peer);
         const uint32_t rowbase = stg_local + r * (kBlockN * 4);       // this row in the staging buffer
         const uint32_t peerbase = xbuf_local + r * (kBlockN * 4);     // this row in the receive buffer
         const uint32_t qbuf = stg_local + q4 * 8192;                  // this warp's 8 KB of the staging buffer (q)
@@ -1016,43 +1043,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
         Cursor cu = cu0;
         Seg sg = seg0;
 
-        // Step C of tile t (of the CTA's stream): partial scores TMEM -> staging ->
-        // the peer's receive buffer.  Every softmax thread takes part in the named
-        // barrier, whatever its `ok`.
-        auto stage_and_send = [&](int t) {
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(&ctl->s_full, t & 1, abort_flag, lim));
-            // the peer has received the previous partial: the staging buffer may be overwritten
-            if (ok && t >= 1) ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->stg_free, (t - 1) & 1, abort_flag, lim));
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t a[32];
-                    tmem_ld32(trow + kTmS + 32 * hh, a);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int uu = 8 * hh + u;
-                        st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
-                                     __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
-                                     __uint_as_float(a[4 * u + 3]));
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&ctl->s_free);  // the S columns may take the next QK
-                fence_proxy_async_smem();
-            }
-            named_bar_sync(3, kSoftmaxThreads);
-            if (r == 0 && ok) {
-                // the peer has read the partial this CTA sent before (its receive buffer is free)
-                if (t >= 1) ok = mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
-                const bool skip_send = fault_kind() == 3 && sg.item == 0 && sg.split == 0 && c == 0 && t == 1;
-                const int rows = exchange_rows<kSparse>(sg, t - g);   // t lies in the current segment
-                const uint32_t off = rows < 0 ? 0u : static_cast<uint32_t>(rows) * (kXBufBytes / 2);
-                if (ok && !skip_send)
-                    bulk_copy_to_peer(xbuf_peer + off, stg_local + off, exchange_bytes(rows), xfull_peer);
-            }
-        };
 
         // ---- persistent: merge of an item cut between CTA pairs ----
         // The pieces of item sg.item are the non-empty shares of pairs q_first,
@@ -1313,11 +1303,11 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     const uint64_t vis_second = a > 0 ? anc >> (kBlockN - a) : 0ull;
                     st_shared_u64x2(vis_addr, vis_first, vis_second);   // kept out of the registers of the tile loop
                 }
-                stage_and_send(g);
                 for (int jj = 0; jj < n; ++jj) {
                     const int gi = g + jj;
                     const int x = gi & 1;
                     // ---- A/B: full scores = own partial (staging) + the peer's (receive buffer) ----
+                    if (ok) ok = mbar_wait(&ctl->staged, gi & 1, abort_flag, lim);
                     if (ok) ok = mbar_wait<true>(&ctl->x_full, gi & 1, abort_flag, lim);
                     float s[kBlockN];
                     if (ok) {
@@ -1348,9 +1338,8 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                             ++posted;
                         }
                         mbar_arrive_remote_relaxed(&ctl->x_empty, peer);
+                        mbar_arrive(&ctl->stg_read);   // the exchange warps may stage the next partial
                     }
-                    // ---- C: ship the next tile's partial scores; its copy overlaps this tile's math ----
-                    if (jj + 1 < n) stage_and_send(gi + 1);
                     // ---- D: this tile's softmax ----
                     // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
                     // the scale is positive, so the row max can be taken on raw scores and the scale
@@ -1592,6 +1581,74 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 mma_commit(&ctl->drain_pv);
                 mbar_wait(&ctl->drain_pv, 0, &zero, lim);
             }
+        }
+
+    } else if (stager_warp) {
+        setmaxnreg_dec<kRegsOther>();
+        // ================= exchange: S (TMEM) -> staging -> the peer's receive buffer =================
+        // Step C of every tile t of the CTA's stream, off the softmax threads' path: as
+        // soon as QK(t) is in TMEM (and the staging buffer is free: the peer has received
+        // partial t - 1 and the softmax threads have read it), the thread of each row
+        // copies its 64 partial scores into the staging buffer, then one thread sends the
+        // tile to the peer once the peer has read partial t - 1, and marks it staged.
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+        const uint32_t stg_local = smem_u32(smem + kOffStaging);
+        const uint32_t xbuf_peer = mapa(smem_u32(smem + kOffXBuf), peer);
+        const uint32_t xfull_peer = mapa(smem_u32(&ctl->x_full), peer);
+        const uint32_t rowbase = stg_local + r * (kBlockN * 4);       // this row in the staging buffer
+        const int sr = static_cast<int>(threadIdx.x) - kStagerWarp0 * 32;   // 0 .. 127
+        bool ok = true;
+        int g = 0;
+        Cursor cu = cu0;
+        Seg sg = seg0;
+        for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
+            const int n = sg.n;
+            if (n <= 0) continue;
+            for (int jj = 0; jj < n; ++jj) {
+                const int t = g + jj;
+                bool w = mbar_wait(&ctl->s_full, t & 1, abort_flag, lim);
+                if (w && t >= 1) w = mbar_wait<true>(&ctl->stg_free, (t - 1) & 1, abort_flag, lim);
+                if (w && t >= 1) w = mbar_wait(&ctl->stg_read, (t - 1) & 1, abort_flag, lim);
+                ok = named_bar_and(7, kSoftmaxThreads, w);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t a[32];
+                    tmem_ld32(trow + kTmS + 32 * hh, a);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int uu = 8 * hh + u;
+                        st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
+                                     __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
+                                     __uint_as_float(a[4 * u + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&ctl->s_free);  // the S columns may take the next QK
+                fence_proxy_async_smem();
+                named_bar_sync(7, kSoftmaxThreads);
+                if (sr == 0) {
+                    // the peer has read the partial this CTA sent before (its receive buffer is free)
+                    bool sent = t < 1 || mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);
+                    const bool skip_send = fault_kind() == 3 && sg.item == 0 && sg.split == 0 && c == 0 && t == 1;
+                    const int rows = exchange_rows<kSparse>(sg, jj);
+                    const uint32_t off = rows < 0 ? 0u : static_cast<uint32_t>(rows) * (kXBufBytes / 2);
+                    if (sent && !skip_send)
+                        bulk_copy_to_peer(xbuf_peer + off, stg_local + off, exchange_bytes(rows), xfull_peer);
+                    mbar_arrive(&ctl->staged);
+                    if (!sent) {
+                        raise_status(p.status, kStatusTimeout);
+                        *abort_flag = 1;
+                    }
+                }
+            }
+            g += n;
+        }
+        if (!ok) {
+            if (sr == 0) raise_status(p.status, kStatusTimeout);
+            *abort_flag = 1;
         }
     }
 

@@ -71,7 +71,7 @@ __device__ void block_exclusive_scan(int n, F f, T* dst, T* warp_sums) {
         if (lane == 31) warp_sums[wid] = x;
         __syncthreads();
         if (wid == 0) {
-            T w = warp_sums[lane];
+            T w = lane < kPrepWarps ? warp_sums[lane] : T(0);
             for (int o = 1; o < 32; o <<= 1) {
                 const T y = __shfl_up_sync(0xffffffffu, w, o);
                 if (lane >= o) w += y;
@@ -81,7 +81,7 @@ __device__ void block_exclusive_scan(int n, F f, T* dst, T* warp_sums) {
         __syncthreads();
         const T before = (wid > 0 ? warp_sums[wid - 1] : T(0)) + x - v;
         if (i < n) dst[i] = carry + before;
-        const T chunk_total = warp_sums[31];
+        const T chunk_total = warp_sums[kPrepWarps - 1];
         __syncthreads();
         carry += chunk_total;
     }

@@ -72,8 +72,11 @@ const char *mla_error_string(int status);
 
 /*
  * Per-device set-up: checks that `device` is an sm_103 GPU, raises the
- * kernels' dynamic shared-memory limit and resolves the driver's tensor-map
- * encoder.  Call once per device, outside stream capture, before the first
+ * kernels' dynamic shared-memory limit, checks that the verify kernels were
+ * compiled with the registers their warpgroups divide among themselves at run
+ * time (MLA_ERR_UNSUPPORTED otherwise: such a build would wait forever) and
+ * resolves the driver's tensor-map encoder.  Call once per device, outside
+ * stream capture, before the first
  * verify call on that device.  Makes `device` current.  Idempotent.  After
  * cudaDeviceReset the device has a new context: call mla_init again before the
  * next call on it (it sets the kernels up again and forgets cached device
@@ -83,9 +86,13 @@ int mla_init(int device);
 
 /*
  * Number of KV splits the verify call will use.  `requested` > 0 is honoured
- * (clamped to [1, MLA_MAX_SPLITS]); 0 picks one from the shape: enough
- * (request, row-tile, split) work units to fill every SM of the current
- * device in whole waves, with at least 16 KV tiles of 64 keys per split.
+ * (clamped to [1, MLA_MAX_SPLITS]); 0 picks a plan from the shape with a
+ * model of the launch: (request, row-tile, split) work units in whole waves
+ * over the SMs of the current device, at least 16 KV tiles of 64 keys per
+ * split; when every unit fits in one wave three times over, as many splits as
+ * still fit in that wave and shorten the chain of dependent tiles (three or
+ * more, merged by the combine pass); or the persistent schedule below (0),
+ * when every request has max_tree tree tokens and the model puts it ahead.
  * When 0 resolves to one split and a request has at least 12 KV tiles, the
  * verify call may also cut the work items of its last, partial round of CTA
  * pairs in two and merge them in the kernel (decided on the device from the

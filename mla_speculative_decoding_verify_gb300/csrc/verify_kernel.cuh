@@ -741,288 +741,288 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // warpgroup's branch starts with its register reallocation: warpgroup 1 (softmax)
     // takes the registers that warpgroups 0 and 2 give back.
     if (warp < kSoftmaxWarp0) {
-    setmaxnreg_dec<kRegsOther>();
-    if (warp == 0 || gather_warp) {
-        // ================= TMA producer(s) =================
-        // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: three
-        // gather warps own 24, 20 and 20 keys of every tile (TMA instructions
-        // issued by the lanes of one warp are serialised, so more warps shorten
-        // the issue time).  Lane l looks up the cache row of the warp's key l;
-        // lane g then loads the warp's keys 4g .. 4g + 3 with four-row gathers
-        // (one box row per key), and each warp posts its share of the tile's bytes
-        // on the stage barrier, so a gathered tile completes exactly like a dense one.  Empty
-        // slots name a row past the end of the cache and read as zeros.  The
-        // lookups run ahead of the copies: before tile jj waits for its stage,
-        // the row of tile jj + 1 is completed and prefetched into L2, and the
-        // block-table entry of tile jj + 2 and the slot value of tile jj + 3 are
-        // loaded; each loaded value is first used one tile later.
-        const uint64_t policy = l2_policy_evict_last();
-        bool ok = true;
-        int issued = 0;   // tiles issued into the ring
-        Cursor cu = cu0;
-        Seg sg = seg0;
-        for (bool have = true, first = true; have && ok;
-             have = next_segment<kSparse, kSched>(p, n_items, cu, sg), first = false) {
-            const int n = sg.n;
-            if (n <= 0) continue;
-            // checked position of a raw slot value of tile jt (slot positions the check
-            // kernel rejected, >= P, are dropped); its block-table load is issued, not waited on
-            [[maybe_unused]] auto translate = [&](int jt, int raw, int& tpos, int& page) {
-                int kind, base;
-                sparse_segment(sg.t0 + jt, sg.nA, sg.nB, kind, base);
-                tpos = (raw < 0 || (kind != 2 && raw >= sg.P)) ? -1 : raw;
-                page = tpos >= 0 ? __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages + tpos / p.page_size)
-                                 : -1;
-            };
-            // cache row from a checked position and its (landed) block-table entry
-            [[maybe_unused]] auto row_of = [&](int tpos, int page) -> int {
-                if (tpos < 0) return -1;
-                if (page < 0 || page >= p.num_pages) {
-                    raise_status(p.status, kStatusBadBlock);
-                    return -1;
-                }
-                return page * p.page_size + tpos % p.page_size;
-            };
-            // this CTA's 576 bytes of a row span five 128-byte lines
-            [[maybe_unused]] auto prefetch_row = [&](int row) {
-                if (row < 0) return;
-                const uint8_t* src = reinterpret_cast<const uint8_t*>(p.kv) + static_cast<long long>(row) * (kDqk * 2);
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == 0 || gather_warp) {
+            // ================= TMA producer(s) =================
+            // Dense: warp 0 loads one 64-row box per chunk of a tile.  Sparse: three
+            // gather warps own 24, 20 and 20 keys of every tile (TMA instructions
+            // issued by the lanes of one warp are serialised, so more warps shorten
+            // the issue time).  Lane l looks up the cache row of the warp's key l;
+            // lane g then loads the warp's keys 4g .. 4g + 3 with four-row gathers
+            // (one box row per key), and each warp posts its share of the tile's bytes
+            // on the stage barrier, so a gathered tile completes exactly like a dense one.  Empty
+            // slots name a row past the end of the cache and read as zeros.  The
+            // lookups run ahead of the copies: before tile jj waits for its stage,
+            // the row of tile jj + 1 is completed and prefetched into L2, and the
+            // block-table entry of tile jj + 2 and the slot value of tile jj + 3 are
+            // loaded; each loaded value is first used one tile later.
+            const uint64_t policy = l2_policy_evict_last();
+            bool ok = true;
+            int issued = 0;   // tiles issued into the ring
+            Cursor cu = cu0;
+            Seg sg = seg0;
+            for (bool have = true, first = true; have && ok;
+                 have = next_segment<kSparse, kSched>(p, n_items, cu, sg), first = false) {
+                const int n = sg.n;
+                if (n <= 0) continue;
+                // checked position of a raw slot value of tile jt (slot positions the check
+                // kernel rejected, >= P, are dropped); its block-table load is issued, not waited on
+                [[maybe_unused]] auto translate = [&](int jt, int raw, int& tpos, int& page) {
+                    int kind, base;
+                    sparse_segment(sg.t0 + jt, sg.nA, sg.nB, kind, base);
+                    tpos = (raw < 0 || (kind != 2 && raw >= sg.P)) ? -1 : raw;
+                    page = tpos >= 0 ? __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages + tpos / p.page_size)
+                                     : -1;
+                };
+                // cache row from a checked position and its (landed) block-table entry
+                [[maybe_unused]] auto row_of = [&](int tpos, int page) -> int {
+                    if (tpos < 0) return -1;
+                    if (page < 0 || page >= p.num_pages) {
+                        raise_status(p.status, kStatusBadBlock);
+                        return -1;
+                    }
+                    return page * p.page_size + tpos % p.page_size;
+                };
+                // this CTA's 576 bytes of a row span five 128-byte lines
+                [[maybe_unused]] auto prefetch_row = [&](int row) {
+                    if (row < 0) return;
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.kv) + static_cast<long long>(row) * (kDqk * 2);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) prefetch_l2(src + kDLatentHalf * 2 * c + 128 * ch);
-                prefetch_l2(src + kDLatent * 2 + kDRopeHalf * 2 * c);
-            };
-            [[maybe_unused]] int raw = -1;   // slot value (tile jj + 3)
-            [[maybe_unused]] int tpos = -1;  // checked position (tile jj + 2) ...
-            [[maybe_unused]] int page = -1;  // ... and its block-table entry, in flight
-            [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
-            [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
-            [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
-            // dense: the block-table entry of the next tile, loaded one tile ahead so that
-            // a freed stage is refilled without a round trip to the table
-            [[maybe_unused]] int pg_next = -1;
-            [[maybe_unused]] auto page_entry = [&](int jt) {
-                return __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages +
-                             (sg.t0 + jt) * kBlockN / p.page_size);
-            };
-            if constexpr (!kSparse) {
-                if (lane == 0) pg_next = page_entry(0);
-            }
-            if constexpr (kSparse) {
-                // the first segment's slot values of tiles 0..2 were loaded before the
-                // set-up; the block-table entries of tiles 0 and 1 are one more round trip
-                if (!first) {
-#pragma unroll
-                    for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(sg, t);
-                }
-                raw = pre_raw[2];
-                int tpos0, page0;
-                translate(0, pre_raw[0], tpos0, page0);
-                translate(1, pre_raw[1], tpos, page);
-                cur = row_of(tpos0, page0);
-                prefetch_row(cur);
-            }
-            for (int jj = 0; jj < n && ok; ++jj) {
-                const int gi = issued;
-                const int st = gi % kStages;
-                [[maybe_unused]] const int pg = pg_next;
+                    for (int ch = 0; ch < 4; ++ch) prefetch_l2(src + kDLatentHalf * 2 * c + 128 * ch);
+                    prefetch_l2(src + kDLatent * 2 + kDRopeHalf * 2 * c);
+                };
+                [[maybe_unused]] int raw = -1;   // slot value (tile jj + 3)
+                [[maybe_unused]] int tpos = -1;  // checked position (tile jj + 2) ...
+                [[maybe_unused]] int page = -1;  // ... and its block-table entry, in flight
+                [[maybe_unused]] int cur = -1;   // cache row of tile jj, -1 for an empty slot
+                [[maybe_unused]] const int oob_row = p.num_pages * p.page_size;
+                [[maybe_unused]] int nxt = -1;   // cache row of tile jj + 1
+                // dense: the block-table entry of the next tile, loaded one tile ahead so that
+                // a freed stage is refilled without a round trip to the table
+                [[maybe_unused]] int pg_next = -1;
+                [[maybe_unused]] auto page_entry = [&](int jt) {
+                    return __ldg(p.block_table + static_cast<long long>(sg.b) * p.max_pages +
+                                 (sg.t0 + jt) * kBlockN / p.page_size);
+                };
                 if constexpr (!kSparse) {
-                    if (lane == 0 && jj + 1 < n) pg_next = page_entry(jj + 1);
+                    if (lane == 0) pg_next = page_entry(0);
                 }
                 if constexpr (kSparse) {
-                    if (jj + 1 < n) {
-                        nxt = row_of(tpos, page);
-                        prefetch_row(nxt);
-                    }
-                    if (jj + 2 < n) {
-                        translate(jj + 2, raw, tpos, page);
-                        raw = slot_raw(sg, jj + 3);
-                    }
-                }
-                if (gi >= kStages) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((gi / kStages) - 1) & 1, abort_flag, lim));
-                    if (!ok) break;
-                }
-                uint8_t* dst = smem + kOffStages + st * kStageBytes;
-                if constexpr (kSparse) {
-                    const uint32_t mask = __ballot_sync(0xffffffffu, cur >= 0);
-                    int y[4];
+                    // the first segment's slot values of tiles 0..2 were loaded before the
+                    // set-up; the block-table entries of tiles 0 and 1 are one more round trip
+                    if (!first) {
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int v = __shfl_sync(0xffffffffu, cur, (4 * lane + t) & 31);
-                        y[t] = v >= 0 ? v : oob_row;
+                        for (int t = 0; t < 3; ++t) pre_raw[t] = slot_raw(sg, t);
                     }
-                    if (lane == 0) {
-                        ctl->slot_mask[st][gw] = mask;
-                        // this warp's share of the stage, 576 bytes per key; releases the mask with the tile
-                        mbar_arrive_expect_tx(&ctl->kv_full[st], static_cast<uint32_t>(nkeys) * (kStageBytes / kBlockN));
+                    raw = pre_raw[2];
+                    int tpos0, page0;
+                    translate(0, pre_raw[0], tpos0, page0);
+                    translate(1, pre_raw[1], tpos, page);
+                    cur = row_of(tpos0, page0);
+                    prefetch_row(cur);
+                }
+                for (int jj = 0; jj < n && ok; ++jj) {
+                    const int gi = issued;
+                    const int st = gi % kStages;
+                    [[maybe_unused]] const int pg = pg_next;
+                    if constexpr (!kSparse) {
+                        if (lane == 0 && jj + 1 < n) pg_next = page_entry(jj + 1);
                     }
-                    __syncwarp();
-                    if (lane < nkeys / 4) {
-                        const int g = key0 / 4 + lane;  // keys 4g .. 4g + 3
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
-                                        kDLatentHalf * static_cast<int>(c) + 64 * ch, y[0], y[1], y[2], y[3], policy);
-                        tma_gather4(dst + 4 * kChunkBytes + 4 * g * 64, &map_rope, &ctl->kv_full[st],
-                                    kDLatent + kDRopeHalf * static_cast<int>(c), y[0], y[1], y[2], y[3], policy);
-                    }
-                    cur = nxt;
-                    ++issued;
-                    __syncwarp();
-                } else {
-                    const int kpos = (sg.t0 + jj) * kBlockN;
-                    if (lane == 0) {
-                        if (pg < 0 || pg >= p.num_pages) raise_status(p.status, kStatusBadBlock);
-                        // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
-                        const int row = pg * p.page_size + (kpos % p.page_size);
-                        mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
-                        for (int ch = 0; ch < 4; ++ch)
-                            tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
-                                        kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
-                        tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
-                                    kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
-                    }
-                    ++issued;
-                    __syncwarp();
-                    if (kpos + kBlockN > sg.L) {
-                        // Last, partial tile: zero the rows past seq_len so that masked
-                        // keys multiply finite values in PV.
-                        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim));
-                        if (!ok) break;
-                        const int kvalid = sg.L - kpos;
-                        uint8_t* base = smem + kOffStages + st * kStageBytes;
-                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
-                            const int u = lane % 8;  // 16-byte unit of the row
-                            for (int ch = 0; ch < 4; ++ch)
-                                *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
-                            if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                    if constexpr (kSparse) {
+                        if (jj + 1 < n) {
+                            nxt = row_of(tpos, page);
+                            prefetch_row(nxt);
                         }
-                        fence_proxy_async_smem();
+                        if (jj + 2 < n) {
+                            translate(jj + 2, raw, tpos, page);
+                            raw = slot_raw(sg, jj + 3);
+                        }
+                    }
+                    if (gi >= kStages) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_empty[st], ((gi / kStages) - 1) & 1, abort_flag, lim));
+                        if (!ok) break;
+                    }
+                    uint8_t* dst = smem + kOffStages + st * kStageBytes;
+                    if constexpr (kSparse) {
+                        const uint32_t mask = __ballot_sync(0xffffffffu, cur >= 0);
+                        int y[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int v = __shfl_sync(0xffffffffu, cur, (4 * lane + t) & 31);
+                            y[t] = v >= 0 ? v : oob_row;
+                        }
+                        if (lane == 0) {
+                            ctl->slot_mask[st][gw] = mask;
+                            // this warp's share of the stage, 576 bytes per key; releases the mask with the tile
+                            mbar_arrive_expect_tx(&ctl->kv_full[st], static_cast<uint32_t>(nkeys) * (kStageBytes / kBlockN));
+                        }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                        if (lane < nkeys / 4) {
+                            const int g = key0 / 4 + lane;  // keys 4g .. 4g + 3
+#pragma unroll
+                            for (int ch = 0; ch < 4; ++ch)
+                                tma_gather4(dst + ch * kChunkBytes + 4 * g * 128, &map_lat, &ctl->kv_full[st],
+                                            kDLatentHalf * static_cast<int>(c) + 64 * ch, y[0], y[1], y[2], y[3], policy);
+                            tma_gather4(dst + 4 * kChunkBytes + 4 * g * 64, &map_rope, &ctl->kv_full[st],
+                                        kDLatent + kDRopeHalf * static_cast<int>(c), y[0], y[1], y[2], y[3], policy);
+                        }
+                        cur = nxt;
+                        ++issued;
+                        __syncwarp();
+                    } else {
+                        const int kpos = (sg.t0 + jj) * kBlockN;
+                        if (lane == 0) {
+                            if (pg < 0 || pg >= p.num_pages) raise_status(p.status, kStatusBadBlock);
+                            // out-of-range pages read as zeros (TMA out-of-bounds fill); the status reports them
+                            const int row = pg * p.page_size + (kpos % p.page_size);
+                            mbar_arrive_expect_tx(&ctl->kv_full[st], kStageBytes);
+                            for (int ch = 0; ch < 4; ++ch)
+                                tma_load_2d(dst + ch * kChunkBytes, &map_lat, &ctl->kv_full[st],
+                                            kDLatentHalf * static_cast<int>(c) + 64 * ch, row, policy);
+                            tma_load_2d(dst + 4 * kChunkBytes, &map_rope, &ctl->kv_full[st],
+                                        kDLatent + kDRopeHalf * static_cast<int>(c), row, policy);
+                        }
+                        ++issued;
+                        __syncwarp();
+                        if (kpos + kBlockN > sg.L) {
+                            // Last, partial tile: zero the rows past seq_len so that masked
+                            // keys multiply finite values in PV.
+                            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim));
+                            if (!ok) break;
+                            const int kvalid = sg.L - kpos;
+                            uint8_t* base = smem + kOffStages + st * kStageBytes;
+                            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int rr = kvalid + lane / 8; rr < kBlockN; rr += 4) {
+                                const int u = lane % 8;  // 16-byte unit of the row
+                                for (int ch = 0; ch < 4; ++ch)
+                                    *reinterpret_cast<float4*>(base + ch * kChunkBytes + rr * 128 + u * 16) = z;
+                                if (u < 4) *reinterpret_cast<float4*>(base + 4 * kChunkBytes + rr * 64 + u * 16) = z;
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ctl->kv_fixed[st]);
+                        }
                     }
                 }
             }
-        }
-        if (!ok) {
-            if (lane == 0) raise_status(p.status, kStatusTimeout);
-            *abort_flag = 1;
-        }
-        // Do not leave the CTA with bulk copies in flight.
-        const int zero = 0;
-        for (int st = 0; st < kStages && st < issued; ++st) {
-            const int last = st + ((issued - 1 - st) / kStages) * kStages;  // last tile issued into stage st
-            mbar_wait(&ctl->kv_full[st], (last / kStages) & 1, &zero, lim);
-        }
-    } else if (warp == 1) {
-        // ================= QK issuer =================
-        const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
-        const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
-        bool ok = true;
-        int g = 0;              // tiles of the earlier segments
-        int segs = 0;           // segments with tiles so far (phases of q_ready)
-        uint32_t fixpar = 0;    // bit st: parity of the next phase of kv_fixed[st]
-        Cursor cu = cu0;
-        Seg sg = seg0;
-        for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
-            const int n = sg.n;
-            if (n <= 0) continue;
-            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, segs & 1, abort_flag, lim));
-            ++segs;
-            if (!ok) break;
-            tc_fence_after();
-            for (int jj = 0; jj < n; ++jj) {
-                const int gi = g + jj;
-                const int st = gi % kStages;
-                const bool tail = !kSparse && (sg.t0 + jj) * kBlockN + kBlockN > sg.L;
-                const bool inject = fault_kind() == 1 && sg.item == 0 && sg.split == 0 && c == 0 && jj == 1;
-                if (inject) {
-                    ok = mbar_wait(&ctl->never, 0, abort_flag, lim);
-                } else if (tail) {
-                    ok = mbar_wait(&ctl->kv_fixed[st], (fixpar >> st) & 1u, abort_flag, lim);
-                    fixpar ^= 1u << st;
-                } else {
-                    ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
-                }
-                // the S columns held tile gi - 1; the softmax threads have read them out
-                if (ok && gi >= 1) ok = mbar_wait(&ctl->s_free, (gi - 1) & 1, abort_flag, lim);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sb = stage0 + st * kStageBytes;
-                    const uint32_t dS = tmem + kTmS;
-                    // one base descriptor per operand; the k-steps add constant byte offsets
-                    const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
-                    const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
-#pragma unroll
-                    for (int k = 0; k < kDLatentHalf / 16; ++k)
-                        mma_ts(dS, tmem + kTmQ + 8 * k, desc_advance(bk, (k >> 2) * kChunkBytes + (k & 3) * 32),
-                               idesc_qk, k > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int k = 0; k < kDRopeHalf / 16; ++k)
-                        mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
-                    mma_commit(&ctl->s_full);
-                }
-                __syncwarp();
+            if (!ok) {
+                if (lane == 0) raise_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
             }
-            g += n;
-        }
-        if (!ok) {
-            if (lane == 0) raise_status(p.status, kStatusTimeout);
-            *abort_flag = 1;
-        }
-        // Wait until every MMA issued by this warp has finished before TMEM is released.
-        const int zero = 0;
-        if (lane == 0) mma_commit(&ctl->drain_qk);
-        __syncwarp();
-        mbar_wait(&ctl->drain_qk, 0, &zero, lim);
-    } else if (warp == kPvWarp) {
-        // ================= PV issuer: O[:, half c] += P * V (P in TMEM) =================
-        const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
-        bool ok = true;
-        int g = 0;
-        Cursor cu = cu0;
-        Seg sg = seg0;
-        for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
-            const int n = sg.n;
-            if (n <= 0) continue;
-            for (int i = 0; i < n && ok; ++i) {
-                const int gi = g + i;
-                const int x = gi & 1;
-                const int st = gi % kStages;
-                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (gi >> 1) & 1, abort_flag, lim));
+            // Do not leave the CTA with bulk copies in flight.
+            const int zero = 0;
+            for (int st = 0; st < kStages && st < issued; ++st) {
+                const int last = st + ((issued - 1 - st) / kStages) * kStages;  // last tile issued into stage st
+                mbar_wait(&ctl->kv_full[st], (last / kStages) & 1, &zero, lim);
+            }
+        } else if (warp == 1) {
+            // ================= QK issuer =================
+            const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
+            const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
+            bool ok = true;
+            int g = 0;              // tiles of the earlier segments
+            int segs = 0;           // segments with tiles so far (phases of q_ready)
+            uint32_t fixpar = 0;    // bit st: parity of the next phase of kv_fixed[st]
+            Cursor cu = cu0;
+            Seg sg = seg0;
+            for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
+                const int n = sg.n;
+                if (n <= 0) continue;
+                ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_ready, segs & 1, abort_flag, lim));
+                ++segs;
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
-                    const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
+                for (int jj = 0; jj < n; ++jj) {
+                    const int gi = g + jj;
+                    const int st = gi % kStages;
+                    const bool tail = !kSparse && (sg.t0 + jj) * kBlockN + kBlockN > sg.L;
+                    const bool inject = fault_kind() == 1 && sg.item == 0 && sg.split == 0 && c == 0 && jj == 1;
+                    if (inject) {
+                        ok = mbar_wait(&ctl->never, 0, abort_flag, lim);
+                    } else if (tail) {
+                        ok = mbar_wait(&ctl->kv_fixed[st], (fixpar >> st) & 1u, abort_flag, lim);
+                        fixpar ^= 1u << st;
+                    } else {
+                        ok = mbar_wait(&ctl->kv_full[st], (gi / kStages) & 1, abort_flag, lim);
+                    }
+                    // the S columns held tile gi - 1; the softmax threads have read them out
+                    if (ok && gi >= 1) ok = mbar_wait(&ctl->s_free, (gi - 1) & 1, abort_flag, lim);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sb = stage0 + st * kStageBytes;
+                        const uint32_t dS = tmem + kTmS;
+                        // one base descriptor per operand; the k-steps add constant byte offsets
+                        const uint64_t bk = smem_desc(sb, 16, 1024, kSwizzle128B);
+                        const uint64_t br = smem_desc(sb + 4 * kChunkBytes, 16, 512, kSwizzle64B);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-                    if (lo) {
+                        for (int k = 0; k < kDLatentHalf / 16; ++k)
+                            mma_ts(dS, tmem + kTmQ + 8 * k, desc_advance(bk, (k >> 2) * kChunkBytes + (k & 3) * 32),
+                                   idesc_qk, k > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int k = 0; k < kDRopeHalf / 16; ++k)
+                            mma_ss(dS, desc_advance(aq_rope, k * 32), desc_advance(br, k * 32), idesc_qk, 1u);
+                        mma_commit(&ctl->s_full);
+                    }
+                    __syncwarp();
+                }
+                g += n;
+            }
+            if (!ok) {
+                if (lane == 0) raise_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
+            }
+            // Wait until every MMA issued by this warp has finished before TMEM is released.
+            const int zero = 0;
+            if (lane == 0) mma_commit(&ctl->drain_qk);
+            __syncwarp();
+            mbar_wait(&ctl->drain_qk, 0, &zero, lim);
+        } else if (warp == kPvWarp) {
+            // ================= PV issuer: O[:, half c] += P * V (P in TMEM) =================
+            const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+            bool ok = true;
+            int g = 0;
+            Cursor cu = cu0;
+            Seg sg = seg0;
+            for (bool have = true; have && ok; have = next_segment<kSparse, kSched>(p, n_items, cu, sg)) {
+                const int n = sg.n;
+                if (n <= 0) continue;
+                for (int i = 0; i < n && ok; ++i) {
+                    const int gi = g + i;
+                    const int x = gi & 1;
+                    const int st = gi % kStages;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (gi >> 1) & 1, abort_flag, lim));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
+                        const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
                         for (int kk = 0; kk < kBlockN / 16; ++kk)
-                            mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                            mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        if (lo) {
+#pragma unroll
+                            for (int kk = 0; kk < kBlockN / 16; ++kk)
+                                mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                        }
+                        mma_commit(&ctl->pv_done[x]);
+                        mma_commit(&ctl->kv_empty[st]);
                     }
-                    mma_commit(&ctl->pv_done[x]);
-                    mma_commit(&ctl->kv_empty[st]);
+                    __syncwarp();
                 }
-                __syncwarp();
+                g += n;
             }
-            g += n;
+            if (!ok) {
+                if (lane == 0) raise_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
+            }
+            const int zero = 0;
+            if (lane == 0) mma_commit(&ctl->drain_pv);
+            __syncwarp();
+            mbar_wait(&ctl->drain_pv, 0, &zero, lim);
         }
-        if (!ok) {
-            if (lane == 0) raise_status(p.status, kStatusTimeout);
-            *abort_flag = 1;
-        }
-        const int zero = 0;
-        if (lane == 0) mma_commit(&ctl->drain_pv);
-        __syncwarp();
-        mbar_wait(&ctl->drain_pv, 0, &zero, lim);
-    }
     } else if (softmax_warp) {
         setmaxnreg_inc<kRegsSoftmax>();
         // ================= softmax / epilogue (thread = row) =================

@@ -186,8 +186,8 @@ struct Ctrl {
     uint64_t kv_fixed[kStages];
     uint64_t s_full;       // QK wrote the S columns (one phase per tile)
     uint64_t s_free;       // the softmax threads read them out (QK may overwrite them)
-    uint64_t p_full[2];    // P of tile j is in shared memory (j & 1 selects the barrier)
-    uint64_t pv_done[2];   // PV of tile j finished (P buffer and O free again)
+    uint64_t p_full[2];    // P of tile j is in its TMEM columns (j & 1 selects the barrier)
+    uint64_t pv_done[2];   // PV of tile j finished (P columns and O free again)
     uint64_t x_full;       // the peer's partial of the next tile landed in the receive buffer (bytes)
     uint64_t x_empty;      // the peer finished reading the partial this CTA sent it
     uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
@@ -509,7 +509,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     // a unit is the CTA's only segment), and writes the merged rows, weighting
     // the splits by their lse and adding them in split order, so the result
     // does not depend on which unit arrives second.  Rows leave through the
-    // warp's 4 KB tile of the P buffers in whole 128-byte lines.  own(part, v)
+    // warp's 4 KB tile of the staging buffer in whole 128-byte lines.  own(part, v)
     // fills v[32] with this unit's normalised columns 32 part .. 32 part + 31 of
     // the thread's row; lse_own is its lse.
     auto two_split_merge = [&](const Seg& sg, auto&& own, float lse_own) {
@@ -1390,7 +1390,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     }
                     ok = __all_sync(0xffffffffu, ok);
                     // PV of the previous tile must be done before O is rescaled and before its
-                    // P buffer is overwritten (it normally finished long ago; the previous
+                    // P columns are overwritten (it normally finished long ago; the previous
                     // segment's last PV was waited for in its epilogue)
                     if (ok && jj > 0)
                         ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(gi - 1) & 1], ((gi - 1) >> 1) & 1,
@@ -1537,7 +1537,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 // The rows go out through shared memory so that every store instruction
                 // writes whole 128-byte lines: the thread of a row puts 32 of its values
                 // into the warp's 4 KB tile (swizzled), then each lane stores 16 bytes of
-                // one of four rows.  The P buffers are free here (PV is done).  A warp's
+                // one of four rows.  The staging buffer is free here (its last copy landed).  A warp's
                 // 32 rows belong to one token, so row_valid is warp-uniform.
                 float* wdst = dst - static_cast<long long>(lane) * kDLatent;   // the warp's first row
                 for (int part = 0; part < kDLatentHalf / 32; ++part) {

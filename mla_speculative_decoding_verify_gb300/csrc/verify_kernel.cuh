@@ -13,20 +13,21 @@
 //     the ancestor bit set of the row's node.
 //   - PV: each CTA accumulates its 256 columns of O = P * c_kv in TMEM (V is
 //     the c_kv latent, so the same shared-memory tile that served as K feeds
-//     PV).  P goes to shared memory as bf16; when a tile carries a large share
-//     of a row's mass a second bf16 "low part" of P is added so the result
-//     keeps close to fp32 weights.
-// Pipeline: the softmax warps read a tile's partial scores out of TMEM as soon
-// as QK has written them and ship them to the peer, then finish the previous
-// tile while the copy is in flight; an S buffer is therefore free again right
-// after it was read, and the QK issuer runs ahead, bounded by the KV ring.  A
-// second MMA warp issues PV as soon as a tile's P is in shared memory.
+//     PV).  P goes to TMEM as bf16 (the A operand of PV); when a tile carries a
+//     large share of a row's mass a second bf16 "low part" of P is added so the
+//     result keeps close to fp32 weights.
+// Pipeline: the exchange warps read a tile's partial scores out of TMEM as soon
+// as QK has written them, stage them in shared memory and ship them to the
+// peer; the S columns are therefore free again right after they were read, and
+// the QK issuer runs ahead, bounded by the four-stage KV ring.  The softmax
+// threads add the two partials, exponentiate and write P; a PV issuer (dense:
+// its own warp; sparse: the QK warp, two tiles behind QK) consumes it.
 // Sparse (top-k) variant (kSparse = true; page "The SMEM Ceiling", section
 // "The Problem Space": each token attends to a top-k selected set of earlier
 // tokens): tree token g sees the prefix positions listed in its topk slots and
 // its ancestor-or-self tree tokens.  A row tile's key sequence is token 0's
 // slots, then token 1's slots, then the tree keys; rows see only their own
-// token's slots.  Two TMA warps gather the rows with four-row tensor gathers
+// token's slots.  Three warps gather the rows with four-row tensor gathers
 // into the same swizzled stage layout (empty slots read as zeros) and record
 // which of the tile's 64 slots are real.
 // Schedules (template parameter kSched):
@@ -41,7 +42,7 @@
 //     across item boundaries.  An item cut between two or more pairs is merged
 //     in the kernel by the last of its pieces to finish (LSE weights, summed in
 //     piece order so that the result does not depend on the order of arrival).
-// TMEM: O [0,256) | q latent half [256,384) | S buffers [384,448), [448,512).
+// TMEM: O [0,256) | q latent half [256,384) | S [384,448) | P [448,480), its low part [480,512).
 #pragma once
 
 #include <cuda.h>
@@ -62,7 +63,7 @@ constexpr int kDLatentHalf = kDLatent / 2;
 constexpr int kDRopeHalf = kDRope / 2;
 constexpr int kStages = 4;
 // Three warpgroups.  Warpgroup 0: warp 0 TMA producer, warp 1 QK MMAs, warp 2 PV MMAs
-// (dense; sparse: warps 0, 2 and 3 gather the KV rows and the softmax issues PV).
+// (dense; sparse: warps 0, 2 and 3 gather the KV rows and warp 1 issues QK and PV).
 // Warpgroup 1 (warps 4..7): softmax, one thread per row.  Warpgroup 2 (warps 8..11):
 // the exchange, partial scores from TMEM through the staging buffer to the peer.
 // Warp w reaches TMEM lanes [32 (w % 4), 32 (w % 4) + 32), so each row-owning
@@ -916,9 +917,38 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 mbar_wait(&ctl->kv_full[st], (last / kStages) & 1, &zero, lim);
             }
         } else if (warp == 1) {
-            // ================= QK issuer =================
+            // ================= QK issuer (sparse: also PV) =================
             const uint32_t idesc_qk = idesc_bf16(128, kBlockN, false, false);
             const uint64_t aq_rope = smem_desc(qrope_addr, 16, 512, kSwizzle64B);
+            // Sparse: the PV warp gathers KV rows, so this warp issues PV of tile gi (the
+            // segment's i-th) once its P is in TMEM, two tiles behind QK (P of tile gi is
+            // ready before the S columns are free for tile gi + 2, so the wait does not
+            // hold QK back), and the segment's last two after its last QK.  Returns false
+            // if the wait ran out.
+            [[maybe_unused]] auto issue_pv = [&](int gi, int i) -> bool {
+                const int x = gi & 1;
+                const int st = gi % kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&ctl->p_full[x], (gi >> 1) & 1, abort_flag, lim))) return false;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
+                    const int lo = *reinterpret_cast<volatile int*>(&ctl->lo_flag[x]);
+                    const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    if (lo) {
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
+                    }
+                    mma_commit(&ctl->pv_done[x]);
+                    mma_commit(&ctl->kv_empty[st]);
+                }
+                __syncwarp();
+                return true;
+            };
             bool ok = true;
             int g = 0;              // tiles of the earlier segments
             int segs = 0;           // segments with tiles so far (phases of q_ready)
@@ -966,6 +996,15 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                         mma_commit(&ctl->s_full);
                     }
                     __syncwarp();
+                    if constexpr (kSparse) {
+                        if (jj > 1 && !issue_pv(gi - 2, jj - 2)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if constexpr (kSparse) {
+                    for (int i = n > 1 ? n - 2 : 0; i < n && ok; ++i) ok = issue_pv(g + i, i);
                 }
                 g += n;
             }
@@ -1464,30 +1503,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                     // weights that PV sees differ from them by unbiased rounding of at most
                     // 2^-9 each, on tiles where no weight exceeds 1/16 of the row's mass.
                     l += psum;
-                    if constexpr (kSparse) {
-                        // PV of this tile, issued by one softmax thread once all 128 rows of P
-                        // are in TMEM (the PV warp gathers KV rows in this variant)
-                        named_bar_sync(5, kSoftmaxThreads);
-                        if (r == 0) {
-                            tc_fence_after();
-                            const uint32_t idesc_pv = idesc_bf16(128, kDLatentHalf, false, true);
-                            const int st = gi % kStages;
-                            const uint64_t bv = smem_desc(stage0 + st * kStageBytes, kChunkBytes, 1024, kSwizzle128B);
-#pragma unroll
-                            for (int kk = 0; kk < kBlockN / 16; ++kk)
-                                mma_ts(tmem + kTmO, tmem + kTmP + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv,
-                                       (jj > 0 || kk > 0) ? 1u : 0u);
-                            if (need_lo) {
-#pragma unroll
-                                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                                    mma_ts(tmem + kTmO, tmem + kTmPLo + 8 * kk, desc_advance(bv, kk * 2048), idesc_pv, 1u);
-                            }
-                            mma_commit(&ctl->pv_done[x]);
-                            mma_commit(&ctl->kv_empty[st]);
-                        }
-                    } else {
-                        mbar_arrive(&ctl->p_full[x]);
-                    }
+                    mbar_arrive(&ctl->p_full[x]);   // the PV issuer (sparse: the QK warp) may go
                 }
                 // ---- epilogue: the segment's last PV ----
                 if (ok) ok = mbar_wait(&ctl->pv_done[(g + n - 1) & 1], ((g + n - 1) >> 1) & 1, abort_flag, lim);
@@ -1573,14 +1589,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                 for (int t = consumed; t < posted; ++t) mbar_wait<true>(&ctl->x_full, t & 1, &zero, lim);
             }
             *abort_flag = 1;
-        }
-        if constexpr (kSparse) {
-            // the PV MMAs this thread issued finish before TMEM is released
-            if (r == 0) {
-                const int zero = 0;
-                mma_commit(&ctl->drain_pv);
-                mbar_wait(&ctl->drain_pv, 0, &zero, lim);
-            }
         }
 
     } else if (stager_warp) {

@@ -193,7 +193,7 @@ struct Ctrl {
     uint64_t x_empty;      // the peer finished reading the partial this CTA sent it
     uint64_t stg_free;     // peer received this CTA's staging buffer (may be overwritten)
     uint64_t staged;       // the exchange warps put the own partial of the next tile in the staging buffer
-    uint64_t stg_read;     // the softmax threads have read it (the exchange warps may overwrite it)
+    uint64_t stg_read[4];  // softmax warp w has read its 32 rows of it (exchange warp w may overwrite them)
     uint64_t q_ready;      // q of the next segment is in TMEM / shared memory (one phase per segment)
     uint64_t drain_qk;
     uint64_t drain_pv;
@@ -446,7 +446,7 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             mbar_init(&ctl->never, 1);
             mbar_init(&ctl->stg_free, 1);
             mbar_init(&ctl->staged, 1);
-            mbar_init(&ctl->stg_read, 1);
+            for (int w = 0; w < 4; ++w) mbar_init(&ctl->stg_read[w], 1);
             ctl->abort = 0;
             mbar_arrive_expect_tx(&ctl->x_full, first_bytes);
             fence_mbar_init_cluster();
@@ -1368,6 +1368,9 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
 #pragma unroll
                         for (int k = 0; k < kBlockN; ++k) s[k] = 0.f;
                     }
+                    // this warp's rows of the staging buffer are read: its exchange warp may stage the next partial
+                    __syncwarp();
+                    if (ok && lane == 0) mbar_arrive(&ctl->stg_read[q4]);
                     // the receive buffer has been read by all 128 threads: let the peer send the next tile
                     named_bar_sync(2, kSoftmaxThreads);
                     if (r == 0 && ok) {
@@ -1377,7 +1380,6 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
                             ++posted;
                         }
                         mbar_arrive_remote_relaxed(&ctl->x_empty, peer);
-                        mbar_arrive(&ctl->stg_read);   // the exchange warps may stage the next partial
                     }
                     // ---- D: this tile's softmax ----
                     // tree mask (tiles that reach the draft tokens only).  Scores stay unscaled here:
@@ -1614,29 +1616,33 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
             if (n <= 0) continue;
             for (int jj = 0; jj < n; ++jj) {
                 const int t = g + jj;
+                // each warp stages its 32 rows as soon as its softmax warp has read them;
+                // the four warps meet once, before the copy
                 bool w = mbar_wait(&ctl->s_full, t & 1, abort_flag, lim);
                 if (w && t >= 1) w = mbar_wait<true>(&ctl->stg_free, (t - 1) & 1, abort_flag, lim);
-                if (w && t >= 1) w = mbar_wait(&ctl->stg_read, (t - 1) & 1, abort_flag, lim);
+                if (w && t >= 1) w = mbar_wait(&ctl->stg_read[q4], (t - 1) & 1, abort_flag, lim);
+                w = __all_sync(0xffffffffu, w);   // the TMEM loads are warp-wide
+                if (w) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t a[32];
+                        tmem_ld32(trow + kTmS + 32 * hh, a);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int uu = 8 * hh + u;
+                            st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
+                                         __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
+                                         __uint_as_float(a[4 * u + 3]));
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&ctl->s_free);  // the S columns may take the next QK
+                    fence_proxy_async_smem();
+                }
                 ok = named_bar_and(7, kSoftmaxThreads, w);
                 if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t a[32];
-                    tmem_ld32(trow + kTmS + 32 * hh, a);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int uu = 8 * hh + u;
-                        st_shared_v4(rowbase + ((uu ^ (r & 7)) << 4), __uint_as_float(a[4 * u]),
-                                     __uint_as_float(a[4 * u + 1]), __uint_as_float(a[4 * u + 2]),
-                                     __uint_as_float(a[4 * u + 3]));
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&ctl->s_free);  // the S columns may take the next QK
-                fence_proxy_async_smem();
-                named_bar_sync(7, kSoftmaxThreads);
                 if (sr == 0) {
                     // the peer has read the partial this CTA sent before (its receive buffer is free)
                     bool sent = t < 1 || mbar_wait<true>(&ctl->x_empty, (t - 1) & 1, abort_flag, lim);

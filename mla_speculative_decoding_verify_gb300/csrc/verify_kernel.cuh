@@ -1596,11 +1596,12 @@ mla_verify_kernel(const __grid_constant__ VerifyParams p, const __grid_constant_
     } else if (stager_warp) {
         setmaxnreg_dec<kRegsOther>();
         // ================= exchange: S (TMEM) -> staging -> the peer's receive buffer =================
-        // Step C of every tile t of the CTA's stream, off the softmax threads' path: as
-        // soon as QK(t) is in TMEM (and the staging buffer is free: the peer has received
-        // partial t - 1 and the softmax threads have read it), the thread of each row
-        // copies its 64 partial scores into the staging buffer, then one thread sends the
-        // tile to the peer once the peer has read partial t - 1, and marks it staged.
+        // Step C of every tile t of the CTA's stream, off the softmax threads' path.  Exchange
+        // warp w owns rows [32w, 32w + 32).  As soon as QK(t) is in TMEM and its rows of the
+        // staging buffer are free (the peer has received partial t - 1 and softmax warp w has
+        // read them), the thread of each row copies its 64 partial scores into the staging
+        // buffer; the four warps then meet, and one thread sends the tile to the peer once
+        // the peer has read partial t - 1, and marks it staged.
         const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
         const uint32_t stg_local = smem_u32(smem + kOffStaging);
         const uint32_t xbuf_peer = mapa(smem_u32(smem + kOffXBuf), peer);
